@@ -1,0 +1,338 @@
+#!/usr/bin/env python3
+"""Causal ring-attention throughput on GB300.
+
+One step = one full ring attention (ra_ring_prepare + ra_ring_attend: shard
+pack, heavy-first block order, all c ring steps and the normalisation) over
+the s128k workload: S = 131072 tokens, c = 16 virtual ranks, zig-zag split,
+causal, batch 1, 16 query heads / 1 KV head, head dim 128, bf16.  The metric
+is algorithmic causal TFLOP/s: 4 * B * Hq * D * S(S+1)/2 FLOP per step over
+the device time of the step.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own independent ring (weak scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal ring-attention TFLOP/s on 1 GB300; % of dense BF16 tensor peak"
+NOMINAL_BF16_DENSE_TFLOPS = 2250.0   # GB300 nominal dense bf16 (no sparsity)
+L2_FLUSH_BYTES = 512 * 1024 * 1024   # > 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="s128k")
+    ap.add_argument("--layout", default=None)
+    ap.add_argument("--mode", default="fused", choices=["fused", "per_step"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_traffic(kernel_src):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "attn_fwd_tc_s128k_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        src = open(os.path.join(ROOT, "context_exact_attention_ra_gb300", "csrc", kernel_src), "rb").read()
+        if d.get("kernel_sha256") == hashlib.sha256(src).hexdigest():
+            return int(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, enabled=True):
+        self.index = index
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(w, layout, seconds, q, k, v):
+    """The float64 oracle on this host's cores over a bounded sample of query
+    rows of the same workload; throughput in algorithmic TFLOP/s."""
+    import numpy as np
+    import oracle
+
+    import torch
+
+    rng = np.random.default_rng(w.seed)
+    pos = np.arange(w.S)
+    h, g = 0, 0                      # query head 0 reads key/value head 0
+    kk = k[:, :, g:g + 1].to(torch.float64).numpy()
+    vv = v[:, :, g:g + 1].to(torch.float64).numpy()
+    done_flop = 0.0
+    rows_done = 0
+    t0 = time.perf_counter()
+    batch = 32
+    while time.perf_counter() - t0 < seconds:
+        rows = np.sort(rng.integers(0, w.S, size=batch))
+        qq = q[:, torch.as_tensor(rows), h:h + 1].to(torch.float64).numpy()
+        oracle.attention_reference(qq, kk, vv, pos[rows], pos, w.causal, w.scale)
+        vis = (rows + 1) if w.causal else np.full(rows.size, w.S)
+        done_flop += 4.0 * w.D * float(vis.sum()) * w.B
+        rows_done += rows.size * w.B
+    el = time.perf_counter() - t0
+    cores = os.cpu_count()
+    return {"value": done_flop / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows_done} random query rows (1 head, float64 full-row masked softmax) of the "
+                      f"{w.name} workload in {el:.1f} s; BLAS threads default to all {cores} cores"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on host cores."""
+    import torch
+    from workloads import WORKLOADS, make_inputs
+
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    layout = args.layout or w.layouts[0]
+    q, k, v, _ = make_inputs(w)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(w, layout, min(per_step, 2.0), q, k, v)
+    vals = [cpu_baseline(w, layout, per_step, q, k, v) for _ in range(args.steps)]
+    val = statistics.median(x["value"] for x in vals)
+    flop = w.flops()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": flop / (val * 1e12) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{w.name}: S={w.S} c={w.c} {layout} causal B={w.B} "
+                                                    f"Hq={w.Hq} Hkv={w.Hkv} D={w.D} {w.dtype}",
+                                        "sample": "random query rows per step (bounded CPU time)"},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": vals[0]["cores"], "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    import context_exact_attention_ra_gb300 as ra
+    from workloads import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = WORKLOADS[args.workload]
+    layout = args.layout or w.layouts[0]
+    q, k, v, _ = make_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    shp = ra.Shape(w.B, w.S, w.S, w.Hq, w.Hkv, w.D, ra.BF16 if w.dtype == "bf16" else ra.F32, w.scale)
+    lay = ra.LAYOUTS[layout]
+    md = ra.MODES[args.mode]
+    ws = torch.empty(ra.ring_workspace_size(shp, w.c, lay, md), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ra.ring_prepare(qd, kd, vd, w.c, lay, ws, scale=w.scale)
+        ra.ring_attend(shp, w.c, lay, w.causal, md, out, lse, ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    ra.device_error()
+    launches_per_step = 2 + (1 if md == ra.MODE_FUSED else w.c + 2)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()   # L2 flush between timed steps (outside the events)
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        ra.ring_prepare(qd, kd, vd, w.c, lay, ws, scale=w.scale)
+        e1.record(stream)
+        ra.ring_attend(shp, w.c, lay, w.causal, md, out, lse, ws)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ra.device_error()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    attend_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flop = w.flops()
+    value = world * flop / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_kind = load_peaks()
+    attn_ms = statistics.mean(attend_ms)
+    achieved = flop / (attn_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": kernel_traffic("attn_tc_sm103.cu") if md == ra.MODE_FUSED else None,
+            "kernel": "attn_fwd_tc_kernel<128>" if md == ra.MODE_FUSED else "attend (per-step launches + merge)",
+            "peak_source": f"{peak_kind} bf16_tflops (burst)",
+            "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+            "frac_of_nominal_dense": achieved / NOMINAL_BF16_DENSE_TFLOPS}
+
+    # end to end through the C ABI with host buffers (copies inside the call)
+    e2e = None
+    if args.e2e_steps > 0:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        oh = torch.empty_like(qh).pin_memory()
+        lh = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32).pin_memory()
+        need = ra.hostio_workspace_size(shp, w.c, lay, md)
+        del ws
+        wsh = torch.empty(need, dtype=torch.uint8, device=dev)
+        ra.ring_forward_hostio(qh, kh, vh, w.c, layout, w.causal, args.mode, w.scale, oh, lh, wsh)
+        times = []
+        for _ in range(args.e2e_steps):
+            flush.zero_()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ra.ring_forward_hostio(qh, kh, vh, w.c, layout, w.causal, args.mode, w.scale, oh, lh, wsh)
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        e2e_ms = statistics.mean(times)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        bi = (q.numel() + k.numel() + v.numel()) * q.element_size()
+        bo = oh.numel() * oh.element_size() + lh.numel() * 4
+        e2e = {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, layout, args.cpu_seconds, q, k, v)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {"workload": f"{w.name}: S={w.S} c={w.c} {layout} causal={w.causal} B={w.B} "
+                                   f"Hq={w.Hq} Hkv={w.Hkv} D={w.D} {w.dtype}",
+                       "mode": args.mode, "l2": "flushed (512 MiB write) before every timed step",
+                       "flop_per_step": flop, "parallelism": f"{w.c} virtual ranks per GPU"},
+            "pct_dense_bf16_peak": {"of_measured": value / world / peak * 100,
+                                    "of_nominal_2250": value / world / NOMINAL_BF16_DENSE_TFLOPS * 100},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "attend_ms": attn_ms,
+            "prepare_ms": statistics.mean(a.elapsed_time(b) for a, b, _ in ev),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

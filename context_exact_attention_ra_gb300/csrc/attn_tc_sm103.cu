@@ -1,0 +1,680 @@
+// Blockwise exact attention with online softmax on the sm_103a tensor cores.
+//
+// One thread block owns 256 query rows (two 128-row tiles Q0, Q1) of one
+// rank and one query head, and walks the key/value tiles of the ring steps
+// [t_begin, t_end) in ring order: at step t it reads the shard of rank
+// (rank - t) mod c ("06 - Sequence / Context Parallelism", section 4: the
+// block a rank holds after t SEND/RECV rounds).  For every key tile it
+//   S_h = Q_h K^T                         (tcgen05.mma, fp32 in tensor memory)
+//   m'  = max(m, rowmax(scale*log2e*S_h)) (causal mask by global position)
+//   P_h = 2^(scale*log2e*S_h - m')        (bf16, written back to tensor memory)
+//   l   = 2^(m - m') l + rowsum(P_h)
+//   O_h = 2^(m - m') O_h + P_h V          (tcgen05.mma, fp32 in tensor memory)
+// which is the online-softmax update with rescaling of the earlier sums
+// whenever a block raises the running maximum (quiz "Sequence Parallelism and
+// Ring Attention", questions 3 and 7).  Key tiles wholly in the future of
+// both query tiles are skipped; tiles that straddle the diagonal are masked
+// element by element.  At the end the state is either written out (per-step
+// mode) or normalised, out = O / l and lse = ln2 (m + log2 l).
+//
+// Warp roles (352 threads):
+//   warps 0-3  softmax for Q0 (warp w reads tensor-memory lanes 32w..32w+31)
+//   warps 4-7  softmax for Q1
+//   warp 8     TMA loads of Q and the K tiles
+//   warp 9     TMA loads of the V tiles
+//   warp 10    tensor-memory allocation and tcgen05.mma issue
+// Pipelines: K and V each have 2 shared-memory stages; the two query tiles
+// ping-pong so that the tensor core multiplies one tile while the softmax of
+// the other runs.  Tensor memory (512 columns): S0 | S1 | O0 | O1, with P_h
+// stored as packed bf16 over the first 64 columns of S_h.
+//
+// Every mbarrier wait is bounded (4 s); a wait that runs out raises an abort
+// flag in shared memory and a bit in the device error word, every role
+// leaves its loop, outstanding tensor-core work and TMA loads are drained
+// (bounded), tensor memory is freed and the block exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "ra_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kWarpK = 8;
+constexpr int kWarpV = 9;
+constexpr int kWarpMma = 10;
+constexpr int kThreads = 11 * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;
+
+template <int D>
+struct Smem {
+  static constexpr int kTileBytes = kTile * D * 2;   // one 128-row bf16 tile
+  static constexpr int kBox = 64;                    // columns per TMA box (128 bytes)
+  static constexpr int kBoxBytes = kTile * kBox * 2;
+  static constexpr int kBoxes = D / kBox;
+  static constexpr int KST = 2;
+  static constexpr int VST = 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kV = kK + KST * kTileBytes;
+  static constexpr int kBar = kV + VST * kTileBytes;
+  static constexpr int bQ = 0;
+  static constexpr int bKFull = 1;
+  static constexpr int bKEmpty = bKFull + KST;
+  static constexpr int bVFull = bKEmpty + KST;
+  static constexpr int bVEmpty = bVFull + VST;
+  static constexpr int bSFull = bVEmpty + VST;
+  static constexpr int bPFull = bSFull + 2;
+  static constexpr int bOFinal = bPFull + 2;
+  static constexpr int bDrain = bOFinal + 1;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kDynamic = kBytes + 1024;     // room to align the base to 1024
+  static_assert(kDynamic <= 232448, "shared memory budget");
+};
+
+// Tensor-memory column of each accumulator.
+__device__ __forceinline__ uint32_t col_S(int h) { return static_cast<uint32_t>(h * 128); }
+__device__ __forceinline__ uint32_t col_O(int h) { return static_cast<uint32_t>(256 + h * 128); }
+
+struct Abort {
+  volatile int* flag;
+  unsigned int* err;
+};
+
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, Abort ab,
+                                           unsigned int code) {
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*ab.flag) return false;
+    if (*reinterpret_cast<volatile unsigned int*>(ab.err) != 0) {
+      *ab.flag = 1;   // another block already gave up: stop early
+      return false;
+    }
+    if (ptx::global_timer_ns() - t0 > kWaitTimeoutNs) {
+      *ab.flag = 1;
+      atomicOr(ab.err, code);
+      return false;
+    }
+  }
+}
+
+// Bounded wait for the phase of `bar` with the given parity.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Abort ab,
+                                         unsigned int code) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, ab, code);
+}
+
+// Wait used on the abort path: ignores the abort flag, shorter limit.
+__device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::global_timer_ns() - t0 > kDrainTimeoutNs) return false;
+  }
+  return true;
+}
+
+// Warp-cooperative min and max of count >= 0 positions (INT_MAX / INT_MIN if empty).
+__device__ __forceinline__ void warp_minmax(const int32_t* pos, int count, int lane, int& mn,
+                                            int& mx) {
+  mn = INT_MAX;
+  mx = INT_MIN;
+  for (int i = lane; i < count; i += 32) {
+    const int p = __ldg(pos + i);
+    mn = min(mn, p);
+    mx = max(mx, p);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+}
+
+// What a block needs to know about its two query tiles.
+struct QTiles {
+  int valid[2];   // rows of each tile inside the rank's shard
+  int mn[2], mx[2];
+  int mx_all;     // max position over both tiles
+};
+
+__device__ __forceinline__ QTiles q_tiles(const AttnParams& p, int rank, int row0, int lane) {
+  QTiles q;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int start = row0 + hh * kTile;
+    q.valid[hh] = max(0, min(kTile, p.n_q - start));
+    warp_minmax(p.q_pos + static_cast<long long>(rank) * p.n_q + start, q.valid[hh], lane,
+                q.mn[hh], q.mx[hh]);
+  }
+  q.mx_all = max(q.mx[0], q.mx[1]);
+  return q;
+}
+
+struct KTile {
+  int valid, mn, mx;
+  bool skip;   // hidden from both query tiles
+};
+
+__device__ __forceinline__ KTile k_tile(const AttnParams& p, int src, int kt, const QTiles& q,
+                                        int lane) {
+  KTile k;
+  const int start = kt * kTile;
+  k.valid = min(kTile, p.n_k - start);
+  warp_minmax(p.k_pos + static_cast<long long>(src) * p.n_k + start, k.valid, lane, k.mn, k.mx);
+  k.skip = p.causal ? (k.mn > q.mx_all) : (q.valid[0] + q.valid[1] == 0);
+  return k;
+}
+
+__device__ __forceinline__ int ring_src(int rank, int t, int c) {
+  int s = (rank - t) % c;
+  return s < 0 ? s + c : s;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  // Align the shared-window address (not the generic one) to 1024 bytes, as
+  // the 128-byte swizzle pattern repeats every 1024 bytes.
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const Abort ab{abort_flag, p.err};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- which problem this block owns -----------------------------------
+  const int b = blockIdx.x / p.Hq;
+  const int h = blockIdx.x % p.Hq;
+  const int g = h / p.G;
+  int yb = blockIdx.y;
+  if (p.block_order != nullptr) yb = p.block_order[yb];
+  const int rank = yb / p.q_blocks_per_rank;
+  const int row0 = (yb % p.q_blocks_per_rank) * kPairRows;   // local row of Q0
+  const int ktiles = (p.n_k + kTile - 1) / kTile;
+
+  // ---- set-up ----------------------------------------------------------
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(L::bQ), 1);
+    for (int s = 0; s < L::KST; ++s) {
+      ptx::mbar_init(bar(L::bKFull + s), 1);
+      ptx::mbar_init(bar(L::bKEmpty + s), 1);
+    }
+    for (int s = 0; s < L::VST; ++s) {
+      ptx::mbar_init(bar(L::bVFull + s), 1);
+      ptx::mbar_init(bar(L::bVEmpty + s), 1);
+    }
+    for (int hh = 0; hh < 2; ++hh) {
+      ptx::mbar_init(bar(L::bSFull + hh), 1);
+      ptx::mbar_init(bar(L::bPFull + hh), 128);
+    }
+    ptx::mbar_init(bar(L::bOFinal), 1);
+    ptx::mbar_init(bar(L::bDrain), 1);
+    // A device error left by an earlier block or launch: do no work.
+    *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.err) != 0) ? 1 : 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpK && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_q);
+    ptx::tma_prefetch_desc(&tm_k);
+  }
+  if (warp == kWarpV && lane == 0) ptx::tma_prefetch_desc(&tm_v);
+  if (warp == kWarpMma) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const QTiles qt = q_tiles(p, rank, row0, lane);
+
+  if (warp == kWarpK || warp == kWarpV) {
+    // ===================== TMA producers ================================
+    const bool is_k = (warp == kWarpK);
+    const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+    const int nst = is_k ? L::KST : L::VST;
+    const int full0 = is_k ? L::bKFull : L::bVFull;
+    const int empty0 = is_k ? L::bKEmpty : L::bVEmpty;
+    const uint32_t stage0 = sbase + (is_k ? L::kK : L::kV);
+    const bool q_issued = is_k && !*abort_flag;
+    if (q_issued && lane == 0) {
+      ptx::mbar_arrive_expect_tx(bar(L::bQ), 2 * L::kTileBytes);
+      for (int hh = 0; hh < 2; ++hh)
+        for (int x = 0; x < L::kBoxes; ++x)
+          ptx::tma_load_4d(sbase + L::kQ + hh * L::kTileBytes + x * L::kBoxBytes, &tm_q,
+                           bar(L::bQ), x * L::kBox, h, rank * p.n_q + row0 + hh * kTile, b);
+    }
+    uint32_t j = 0;
+    bool ok = !*abort_flag;
+    for (int t = p.t_begin; t < p.t_end && ok; ++t) {
+      const int src = ring_src(rank, t, p.c);
+      for (int kt = 0; kt < ktiles; ++kt) {
+        const KTile k = k_tile(p, src, kt, qt, lane);
+        if (k.skip) continue;
+        if (lane == 0) {
+          const int s = static_cast<int>(j % nst);
+          const uint32_t n = j / nst;
+          if (n > 0) ok = wait_bar(bar(empty0 + s), (n - 1) & 1u, ab, kErrTimeoutEmpty);
+          if (ok) {
+            ptx::mbar_arrive_expect_tx(bar(full0 + s), L::kTileBytes);
+            for (int x = 0; x < L::kBoxes; ++x)
+              ptx::tma_load_4d(stage0 + s * L::kTileBytes + x * L::kBoxBytes, map,
+                               bar(full0 + s), x * L::kBox, g, src * p.n_k + kt * kTile, b);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++j;
+      }
+    }
+    if (lane == 0 && *abort_flag) {
+      // Let the loads still in flight land before the block exits.
+      if (q_issued) wait_bar_drain(bar(L::bQ), 0);
+      for (int s = 0; s < nst; ++s) {
+        const uint32_t issued = (j > static_cast<uint32_t>(s)) ? (j - 1 - s) / nst + 1 : 0;
+        if (issued > 0) wait_bar_drain(bar(full0 + s), (issued - 1) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ===================== tensor-core issue ============================
+    constexpr uint32_t idS = ptx::idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t idPV = ptx::idesc_bf16_f32(128, D, true);
+    bool ok = true;
+    bool issued_any = false;
+    if (lane == 0) ok = wait_bar(bar(L::bQ), 0, ab, kErrTimeoutQ);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+
+    auto issue_S = [&](int hh, int ks) {
+      const uint32_t qa = sbase + L::kQ + hh * L::kTileBytes;
+      const uint32_t ka = sbase + L::kK + ks * L::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * L::kBoxBytes + (kk % 4) * 32;
+        ptx::tc_mma_ss(tmem + col_S(hh), ptx::smem_desc_sw128(qa + off, 16, 1024),
+                       ptx::smem_desc_sw128(ka + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_PV = [&](int hh, int vs) {
+      const uint32_t va = sbase + L::kV + vs * L::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        ptx::tc_mma_ts(tmem + col_O(hh), tmem + col_S(hh) + kk * 8,
+                       ptx::smem_desc_sw128(va + kk * 16 * 128, L::kBoxBytes, 1024), idPV, 1u);
+      }
+    };
+
+    uint32_t j = 0;
+    for (int t = p.t_begin; t < p.t_end && ok; ++t) {
+      const int src = ring_src(rank, t, p.c);
+      unsigned long long nfull = 0, npart = 0, nskip = 0;
+      for (int kt = 0; kt < ktiles; ++kt) {
+        const KTile k = k_tile(p, src, kt, qt, lane);
+        if (p.work != nullptr) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if (qt.valid[hh] == 0) continue;
+            if (!p.causal || k.mx <= qt.mn[hh]) ++nfull;
+            else if (k.mn > qt.mx[hh]) ++nskip;
+            else ++npart;
+          }
+        }
+        if (k.skip) continue;
+        if (lane == 0) {
+          const int ks = static_cast<int>(j % L::KST);
+          ok = wait_bar(bar(L::bKFull + ks), (j / L::KST) & 1u, ab, kErrTimeoutK);
+          if (ok) ptx::tc_fence_after_sync();
+          if (ok && j == 0) {
+            for (int hh = 0; hh < 2; ++hh) {
+              issue_S(hh, ks);
+              ptx::tc_commit(bar(L::bSFull + hh));
+            }
+            issued_any = true;
+          } else if (ok) {
+            const uint32_t jp = j - 1;
+            const int vs = static_cast<int>(jp % L::VST);
+            ok = wait_bar(bar(L::bVFull + vs), (jp / L::VST) & 1u, ab, kErrTimeoutV);
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              ok = wait_bar(bar(L::bPFull + hh), jp & 1u, ab, kErrTimeoutP);
+              if (!ok) break;
+              ptx::tc_fence_after_sync();
+              issue_PV(hh, vs);
+              issue_S(hh, ks);
+              ptx::tc_commit(bar(L::bSFull + hh));
+            }
+            if (ok) ptx::tc_commit(bar(L::bVEmpty + vs));
+          }
+          if (ok) ptx::tc_commit(bar(L::bKEmpty + ks));
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++j;
+      }
+      if (p.work != nullptr && lane == 0 && ok) {
+        ra_work* w = p.work + static_cast<long long>(rank) * p.c + t;
+        atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_full), nfull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_partial), npart);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_skipped), nskip);
+      }
+    }
+    if (lane == 0) {
+      if (ok && j > 0) {
+        const uint32_t jp = j - 1;
+        const int vs = static_cast<int>(jp % L::VST);
+        ok = wait_bar(bar(L::bVFull + vs), (jp / L::VST) & 1u, ab, kErrTimeoutV);
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          ok = wait_bar(bar(L::bPFull + hh), jp & 1u, ab, kErrTimeoutP);
+          if (!ok) break;
+          ptx::tc_fence_after_sync();
+          issue_PV(hh, vs);
+        }
+        if (ok) ptx::tc_commit(bar(L::bOFinal));
+      }
+      if (!ok && issued_any) {
+        // Drain the tensor core before tensor memory is released.
+        ptx::tc_commit(bar(L::bDrain));
+        if (!wait_bar_drain(bar(L::bDrain), 0)) atomicOr(p.err, kErrTimeoutDrain);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ===================== softmax warpgroups ===========================
+    const int hh = warp >> 2;                 // query tile of this warpgroup
+    const int wq = warp & 3;                  // lane quarter of tensor memory
+    const int r = wq * 32 + lane;             // row inside the tile
+    const int local_row = row0 + hh * kTile + r;
+    const bool row_ok = r < qt.valid[hh];
+    const long long qrow = static_cast<long long>(rank) * p.n_q + local_row;
+    const long long R = static_cast<long long>(p.c) * p.n_q;
+    const int qpos = row_ok ? __ldg(p.q_pos + qrow) : INT_MIN;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + col_S(hh);
+    const uint32_t tO = tmem + lane_base + col_O(hh);
+    const float sl2 = p.scale_log2;
+
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    {
+      // Initial state: loaded (per-step mode) or empty.
+      const float* src_o = nullptr;
+      if (p.load_state && row_ok) {
+        const long long si = (static_cast<long long>(b) * p.Hq + h) * R + qrow;
+        m_run = p.m_state[si];
+        l_run = p.l_state[si];
+        src_o = p.o_state + ((static_cast<long long>(b) * R + qrow) * p.Hq + h) * D;
+      }
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        if (src_o != nullptr) {
+          const float4* s4 = reinterpret_cast<const float4*>(src_o + cc * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 f = s4[i];
+            u[4 * i + 0] = __float_as_uint(f.x);
+            u[4 * i + 1] = __float_as_uint(f.y);
+            u[4 * i + 2] = __float_as_uint(f.z);
+            u[4 * i + 3] = __float_as_uint(f.w);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        ptx::tmem_st32(tO + cc * 32, u);
+      }
+      ptx::tmem_wait_st();
+    }
+
+    uint32_t j = 0;
+    bool ok = true;
+    for (int t = p.t_begin; t < p.t_end && ok; ++t) {
+      const int src = ring_src(rank, t, p.c);
+      const int32_t* kpos_src = p.k_pos + static_cast<long long>(src) * p.n_k;
+      unsigned long long pairs = 0;
+      for (int kt = 0; kt < ktiles; ++kt) {
+        const KTile k = k_tile(p, src, kt, qt, lane);
+        if (k.skip) continue;
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bSFull + hh), j & 1u, ab, kErrTimeoutS));
+        if (!ok) break;
+        ptx::tc_fence_after_sync();
+        const bool masked = (k.valid < kTile) || (p.causal && k.mx > qt.mn[hh]);
+        const int32_t* kp = kpos_src + kt * kTile;
+
+        // pass 1: row maximum of the visible scores
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t u[32];
+          ptx::tmem_ld32(tS + cc * 32, u);
+          if (masked) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int col = cc * 32 + i;
+              const bool vis = col < k.valid && (!p.causal || __ldg(kp + min(col, k.valid - 1)) <= qpos);
+              if (vis) mx = fmaxf(mx, __uint_as_float(u[i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(u[i]));
+          }
+        }
+        const float m_new = fmaxf(m_run, mx * sl2);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+
+        // pass 2: probabilities, their sum, and P (bf16) over S's columns
+        float sum = 0.f;
+        unsigned int nvis = 0;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t u[32];
+          ptx::tmem_ld32(tS + cc * 32, u);
+          float pr[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float e = ptx::ex2(fmaf(__uint_as_float(u[i]), sl2, -m_use));
+            bool vis = true;
+            if (masked) {
+              const int col = cc * 32 + i;
+              vis = col < k.valid && (!p.causal || __ldg(kp + min(col, k.valid - 1)) <= qpos);
+            }
+            pr[i] = vis ? e : 0.f;
+            nvis += vis ? 1u : 0u;
+            sum += pr[i];
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+          ptx::tmem_st16(tS + cc * 16, pk);
+        }
+        const float alpha = (m_run == m_new) ? 1.f : ptx::ex2(m_run - m_new);
+        l_run = l_run * alpha + sum;
+        // rescale the accumulator when the running maximum rose
+        const bool need = (alpha != 1.f) && (m_run != -INFINITY);
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t u[32];
+            ptx::tmem_ld32(tO + cc * 32, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            ptx::tmem_st32(tO + cc * 32, u);
+          }
+        }
+        m_run = m_new;
+        if (row_ok) pairs += nvis;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before_sync();
+        ptx::mbar_arrive(bar(L::bPFull + hh));
+        ++j;
+      }
+      if (p.work != nullptr && ok) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
+        if (lane == 0 && pairs > 0) {
+          ra_work* w = p.work + static_cast<long long>(rank) * p.c + t;
+          atomicAdd(reinterpret_cast<unsigned long long*>(&w->pairs), pairs);
+        }
+      }
+    }
+
+    // ---- epilogue ---------------------------------------------------------
+    if (ok && j > 0) ok = __all_sync(0xffffffffu, wait_bar(bar(L::bOFinal), 0, ab, kErrTimeoutO));
+    if (ok) {
+      ptx::tc_fence_after_sync();
+      if (p.finalize) {
+        const int orow = row_ok ? qpos : 0;
+        const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                             ((static_cast<long long>(b) * p.S_out + orow) * p.Hq + h) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t u[32];
+          ptx::tmem_ld32(tO + cc * 32, u);
+          if (row_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv_l, __uint_as_float(u[8 * i + 1]) * inv_l);
+              w.y = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv_l, __uint_as_float(u[8 * i + 3]) * inv_l);
+              w.z = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv_l, __uint_as_float(u[8 * i + 5]) * inv_l);
+              w.w = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv_l, __uint_as_float(u[8 * i + 7]) * inv_l);
+              d4[i] = w;
+            }
+          }
+        }
+        if (row_ok && p.lse != nullptr) {
+          const float lse = (l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+          p.lse[(static_cast<long long>(b) * p.Hq + h) * p.S_out + orow] = lse;
+        }
+      }
+      if (p.store_state) {
+        float* dst = p.o_state + ((static_cast<long long>(b) * R + qrow) * p.Hq + h) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t u[32];
+          ptx::tmem_ld32(tO + cc * 32, u);
+          if (row_ok) {
+            float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                  __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+          }
+        }
+        if (row_ok) {
+          const long long si = (static_cast<long long>(b) * p.Hq + h) * R + qrow;
+          p.m_state[si] = m_run;
+          p.l_state[si] = l_run;
+        }
+      }
+    }
+  }
+
+  // ---- teardown -------------------------------------------------------------
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and launch.
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(int* err) {
+  static EncodeTiledFn fn = nullptr;
+  static int status = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || f == nullptr)
+      status = (e != cudaSuccess) ? static_cast<int>(e) : static_cast<int>(cudaErrorNotSupported);
+    else
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  *err = status;
+  return fn;
+}
+
+// [B][rows][H][D] bf16 tensor, boxes of 64 columns x 1 head x 128 rows.
+int make_map(CUtensorMap* map, const void* base, int B, long long rows, int H, int D) {
+  int err = 0;
+  EncodeTiledFn fn = encode_fn(&err);
+  if (fn == nullptr) return err ? err : static_cast<int>(cudaErrorNotSupported);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(rows) * H * D * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(cudaErrorInvalidValue);
+}
+
+template <int D>
+int launch_d(const AttnParams& p, const void* q, const void* k, const void* v,
+             long long q_rows_total, long long k_rows_total, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  std::memset(&mq, 0, sizeof(mq));
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  int e = make_map(&mq, q, p.B, q_rows_total, p.Hq, D);
+  if (!e) e = make_map(&mk, k, p.B, k_rows_total, p.Hkv, D);
+  if (!e) e = make_map(&mv, v, p.B, k_rows_total, p.Hkv, D);
+  if (e) return e;
+  const int smem = Smem<D>::kDynamic;
+  cudaError_t ce = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (ce != cudaSuccess) return static_cast<int>(ce);
+  dim3 grid(static_cast<unsigned>(p.B * p.Hq), static_cast<unsigned>(p.c * p.q_blocks_per_rank));
+  attn_fwd_tc_kernel<D><<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_attn_tc(const AttnParams& p, const void* q, const void* k, const void* v,
+                   long long q_rows_total, long long k_rows_total, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.D == 128) return launch_d<128>(p, q, k, v, q_rows_total, k_rows_total, s);
+  if (p.D == 64) return launch_d<64>(p, q, k, v, q_rows_total, k_rows_total, s);
+  return static_cast<int>(cudaErrorInvalidValue);
+}
+
+}  // namespace ra

@@ -1,0 +1,450 @@
+// C ABI of the ring-attention library: argument checks, workspace layout,
+// and the order of launches.  Every check runs on the host before anything
+// is launched.
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "ra.h"
+#include "ra_internal.h"
+
+namespace {
+
+using ra::AttnParams;
+
+constexpr double kLn2 = 0.69314718055994530942;
+constexpr double kLog2e = 1.44269504088896340736;
+constexpr size_t kAlign = 256;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int elem_bytes(int dtype) { return dtype == RA_F32 ? 4 : 2; }
+
+ra_status cuda_status(int e) { return e == 0 ? RA_OK : RA_ERR_CUDA; }
+
+ra_status check_shape(const ra_shape& s) {
+  if (s.B < 0 || s.Sq < 0 || s.Sk < 0 || s.Hq <= 0 || s.Hkv <= 0) return RA_ERR_INVALID;
+  if (s.Hq % s.Hkv != 0) return RA_ERR_INVALID;
+  if (s.dtype != RA_BF16 && s.dtype != RA_F32) return RA_ERR_UNSUPPORTED;
+  if (s.D != 64 && s.D != 128) return RA_ERR_UNSUPPORTED;
+  if (!std::isfinite(s.scale) || !(s.scale > 0.f)) return RA_ERR_INVALID;
+  // Index arithmetic in the kernels is 64-bit; grid x holds B*Hq.
+  if (static_cast<long long>(s.B) * s.Hq > 0x7fffffffLL) return RA_ERR_UNSUPPORTED;
+  return RA_OK;
+}
+
+ra_status check_ring(const ra_shape& s, int c, int layout) {
+  ra_status st = check_shape(s);
+  if (st != RA_OK) return st;
+  if (s.Sq != s.Sk) return RA_ERR_INVALID;
+  if (c < 1) return RA_ERR_INVALID;
+  if (layout != RA_CONTIGUOUS && layout != RA_ZIGZAG) return RA_ERR_INVALID;
+  const long long S = s.Sq;
+  if (layout == RA_CONTIGUOUS && S % c != 0) return RA_ERR_INVALID;
+  if (layout == RA_ZIGZAG && S % (2LL * c) != 0) return RA_ERR_INVALID;
+  return RA_OK;
+}
+
+int rows_per_block(int dtype) { return dtype == RA_BF16 ? ra::kPairRows : ra::kTile; }
+
+int blocks_per_rank(const ra_shape& s, int n_q) {
+  const int rpb = rows_per_block(s.dtype);
+  return (n_q + rpb - 1) / rpb;
+}
+
+// Regions of a ring workspace, as byte offsets from its base.
+struct RingWs {
+  size_t qp, kp, vp, pos, order, work, o, m, l, total;
+};
+
+RingWs ring_ws(const ra_shape& s, int c, int mode) {
+  RingWs w;
+  const size_t eb = static_cast<size_t>(elem_bytes(s.dtype));
+  const size_t S = static_cast<size_t>(s.Sq), B = static_cast<size_t>(s.B);
+  const size_t D = static_cast<size_t>(s.D);
+  const int n = c > 0 ? s.Sq / c : 0;
+  const size_t nblocks = static_cast<size_t>(c) * blocks_per_rank(s, n);
+  size_t off = 0;
+  w.qp = off;    off = round_up(off + B * S * s.Hq * D * eb);
+  w.kp = off;    off = round_up(off + B * S * s.Hkv * D * eb);
+  w.vp = off;    off = round_up(off + B * S * s.Hkv * D * eb);
+  w.pos = off;   off = round_up(off + S * sizeof(int32_t));
+  w.order = off; off = round_up(off + nblocks * sizeof(int32_t));
+  w.work = off;  off = round_up(off + static_cast<size_t>(c) * c * sizeof(ra_work));
+  if (mode == RA_MODE_PER_STEP) {
+    w.o = off;   off = round_up(off + B * S * s.Hq * D * sizeof(float));
+    w.m = off;   off = round_up(off + B * s.Hq * S * sizeof(float));
+    w.l = off;   off = round_up(off + B * s.Hq * S * sizeof(float));
+  } else {
+    w.o = w.m = w.l = 0;
+  }
+  w.total = off;
+  return w;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+AttnParams base_params(const ra_shape& s, int c, int n_q, int n_k, int causal) {
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.G = s.Hq / s.Hkv;
+  p.D = s.D;
+  p.c = c;
+  p.n_q = n_q;
+  p.n_k = n_k;
+  p.q_blocks_per_rank = blocks_per_rank(s, n_q);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(s.scale) * kLog2e);
+  return p;
+}
+
+ra_status launch_attn(const AttnParams& p, const ra_shape& s, long long q_rows, long long k_rows,
+                      void* stream) {
+  if (static_cast<long long>(p.c) * p.q_blocks_per_rank > 65535) return RA_ERR_UNSUPPORTED;
+  int e = (s.dtype == RA_BF16) ? ra::launch_attn_tc(p, p.q, p.k, p.v, q_rows, k_rows, stream)
+                               : ra::launch_attn_f32(p, stream);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ra_status_string(int status) {
+  switch (status) {
+    case RA_OK: return "ok";
+    case RA_ERR_INVALID: return "invalid argument";
+    case RA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case RA_ERR_CUDA: return "CUDA error";
+    case RA_ERR_TIMEOUT: return "device wait timed out";
+    case RA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+const char* ra_version(void) { return "ra-gb300 0.1 sm_103a"; }
+
+ra_status ra_state_init(ra_shape shp, float* o, float* m, float* l, ra_stream_t stream) {
+  ra_status st = check_shape(shp);
+  if (st != RA_OK) return st;
+  if (shp.B == 0 || shp.Sq == 0) return RA_OK;
+  if (o == nullptr || m == nullptr || l == nullptr || !aligned16(o)) return RA_ERR_INVALID;
+  return cuda_status(ra::launch_state_init(shp.B, shp.Sq, shp.Hq, shp.D, o, m, l, stream));
+}
+
+ra_status ra_block_attn(const void* q, const void* k, const void* v, const int32_t* q_pos,
+                        const int32_t* k_pos, int causal, ra_shape shp, float* o, float* m,
+                        float* l, ra_work* work, ra_stream_t stream) {
+  ra_status st = check_shape(shp);
+  if (st != RA_OK) return st;
+  if (shp.B == 0 || shp.Sq == 0 || shp.Sk == 0) return RA_OK;
+  if (!q || !k || !v || !q_pos || !k_pos || !o || !m || !l) return RA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(work) & 7u) != 0) return RA_ERR_INVALID;
+  int err = 0;
+  unsigned int* ew = ra::device_error_word(&err);
+  if (ew == nullptr) return RA_ERR_CUDA;
+  AttnParams p = base_params(shp, 1, shp.Sq, shp.Sk, causal);
+  p.q_pos = q_pos;
+  p.k_pos = k_pos;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.t_begin = 0;
+  p.t_end = 1;
+  p.o_state = o;
+  p.m_state = m;
+  p.l_state = l;
+  p.load_state = 1;
+  p.store_state = 1;
+  p.finalize = 0;
+  p.work = work;
+  p.err = ew;
+  return launch_attn(p, shp, shp.Sq, shp.Sk, stream);
+}
+
+ra_status ra_lse_merge(int P, const float* const* outs, const float* const* ms,
+                       const float* const* ls, ra_shape shp, void* out, float* lse,
+                       ra_stream_t stream) {
+  ra_status st = check_shape(shp);
+  if (st != RA_OK) return st;
+  if (P < 1 || P > RA_MERGE_MAX_PARTIALS) return RA_ERR_INVALID;
+  if (!outs || !ms || !ls) return RA_ERR_INVALID;
+  if (shp.B == 0 || shp.Sq == 0) return RA_OK;
+  if (out == nullptr || !aligned16(out)) return RA_ERR_INVALID;
+  ra::MergeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.P = P;
+  for (int i = 0; i < P; ++i) {
+    if (!outs[i] || !ms[i] || !ls[i] || !aligned16(outs[i])) return RA_ERR_INVALID;
+    a.outs[i] = outs[i];
+    a.ms[i] = ms[i];
+    a.ls[i] = ls[i];
+  }
+  return cuda_status(ra::launch_merge(a, shp.B, shp.Sq, shp.Hq, shp.D, shp.dtype, out, lse,
+                                      nullptr, shp.Sq, stream));
+}
+
+size_t ra_ring_forward_workspace_size(ra_shape shp, int c, int layout, int mode) {
+  if (check_ring(shp, c, layout) != RA_OK) return 0;
+  if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return 0;
+  return ring_ws(shp, c, mode).total;
+}
+
+ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape shp, int c,
+                          int layout, void* workspace, size_t ws_bytes, ra_stream_t stream) {
+  ra_status st = check_ring(shp, c, layout);
+  if (st != RA_OK) return st;
+  if (shp.B == 0 || shp.Sq == 0) return RA_OK;
+  if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return RA_ERR_INVALID;
+  const RingWs w = ring_ws(shp, c, RA_MODE_FUSED);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      ws_bytes < w.total)
+    return RA_ERR_WORKSPACE;
+  int e = ra::launch_pack(q, k, v, shp.B, shp.Sq, shp.Hq, shp.Hkv, shp.D, elem_bytes(shp.dtype),
+                          c, layout, at<void>(workspace, w.qp), at<void>(workspace, w.kp),
+                          at<void>(workspace, w.vp), at<int32_t>(workspace, w.pos), stream);
+  if (e) return RA_ERR_CUDA;
+  // Heavy-first block order (used by causal calls): depends on positions only.
+  const int n = shp.Sq / c;
+  const int total_blocks = c * blocks_per_rank(shp, n);
+  if (total_blocks > 1 && total_blocks <= ra::kMaxOrderedBlocks) {
+    e = ra::launch_block_order(at<int32_t>(workspace, w.pos), c, n, rows_per_block(shp.dtype),
+                               blocks_per_rank(shp, n), at<int32_t>(workspace, w.order), stream);
+    if (e) return RA_ERR_CUDA;
+  }
+  return RA_OK;
+}
+
+ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, void* out,
+                         float* lse, void* workspace, size_t ws_bytes, int count_work,
+                         ra_stream_t stream) {
+  ra_status st = check_ring(shp, c, layout);
+  if (st != RA_OK) return st;
+  if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (shp.B == 0 || shp.Sq == 0) return RA_OK;
+  if (out == nullptr || !aligned16(out)) return RA_ERR_INVALID;
+  const RingWs w = ring_ws(shp, c, mode);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      ws_bytes < w.total)
+    return RA_ERR_WORKSPACE;
+  int err = 0;
+  unsigned int* ew = ra::device_error_word(&err);
+  if (ew == nullptr) return RA_ERR_CUDA;
+
+  const int S = shp.Sq;
+  const int n = S / c;
+  AttnParams p = base_params(shp, c, n, n, causal);
+  p.q_pos = at<int32_t>(workspace, w.pos);
+  p.k_pos = p.q_pos;
+  p.q = at<void>(workspace, w.qp);
+  p.k = at<void>(workspace, w.kp);
+  p.v = at<void>(workspace, w.vp);
+  p.err = ew;
+  p.out = out;
+  p.lse = lse;
+  p.S_out = S;
+  if (count_work) {
+    p.work = at<ra_work>(workspace, w.work);
+    int e = ra::launch_zero(p.work, static_cast<size_t>(c) * c * sizeof(ra_work), stream);
+    if (e) return RA_ERR_CUDA;
+  }
+  const int total_blocks = c * p.q_blocks_per_rank;
+  if (causal && total_blocks <= ra::kMaxOrderedBlocks && total_blocks > 1)
+    p.block_order = at<int32_t>(workspace, w.order);   // written by ra_ring_prepare
+  if (mode == RA_MODE_FUSED) {
+    p.t_begin = 0;
+    p.t_end = c;
+    p.finalize = 1;
+    return launch_attn(p, shp, S, S, stream);
+  }
+  // Per-step: state in the workspace, one launch per ring step, then out / l.
+  p.o_state = at<float>(workspace, w.o);
+  p.m_state = at<float>(workspace, w.m);
+  p.l_state = at<float>(workspace, w.l);
+  p.load_state = 1;
+  p.store_state = 1;
+  p.finalize = 0;
+  int e = ra::launch_state_init(shp.B, S, shp.Hq, shp.D, p.o_state, p.m_state, p.l_state, stream);
+  if (e) return RA_ERR_CUDA;
+  for (int t = 0; t < c; ++t) {
+    p.t_begin = t;
+    p.t_end = t + 1;
+    st = launch_attn(p, shp, S, S, stream);
+    if (st != RA_OK) return st;
+  }
+  ra::MergeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.P = 1;
+  a.outs[0] = p.o_state;
+  a.ms[0] = p.m_state;
+  a.ls[0] = p.l_state;
+  return cuda_status(ra::launch_merge(a, shp.B, S, shp.Hq, shp.D, shp.dtype, out, lse, p.q_pos, S,
+                                      stream));
+}
+
+ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const void* workspace,
+                            size_t ws_bytes, ra_work* host_per_rank_step, ra_stream_t stream) {
+  ra_status st = check_ring(shp, c, layout);
+  if (st != RA_OK) return st;
+  if (host_per_rank_step == nullptr) return RA_ERR_INVALID;
+  const RingWs w = ring_ws(shp, c, mode);
+  if (workspace == nullptr || ws_bytes < w.total) return RA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RA_ERR_CUDA;
+  if (cudaMemcpy(host_per_rank_step, static_cast<const char*>(workspace) + w.work,
+                 static_cast<size_t>(c) * c * sizeof(ra_work), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return RA_ERR_CUDA;
+  return RA_OK;
+}
+
+ra_status ra_device_error(ra_stream_t stream) {
+  unsigned int v = 0;
+  int e = ra::read_and_clear_error(stream, &v);
+  if (e) return RA_ERR_CUDA;
+  return v ? RA_ERR_TIMEOUT : RA_OK;
+}
+
+ra_status ra_schedule(int c, int32_t* table) {
+  if (c < 1 || table == nullptr) return RA_ERR_INVALID;
+  for (int t = 0; t < c; ++t)
+    for (int i = 0; i < c; ++i) table[static_cast<long long>(t) * c + i] = ((i - t) % c + c) % c;
+  return RA_OK;
+}
+
+ra_status ra_shard_positions(int S, int c, int layout, int32_t* pos) {
+  ra_shape s{1, S, S, 1, 1, 128, RA_BF16, 1.f};
+  ra_status st = check_ring(s, c, layout);
+  if (st != RA_OK) return st;
+  if (pos == nullptr && S > 0) return RA_ERR_INVALID;
+  ra::shard_positions(S, c, layout, pos);
+  return RA_OK;
+}
+
+ra_status ra_work_expected(int S, int c, int layout, int causal, ra_work* out) {
+  ra_shape s{1, S, S, 1, 1, 128, RA_BF16, 1.f};
+  ra_status st = check_ring(s, c, layout);
+  if (st != RA_OK) return st;
+  if (out == nullptr) return RA_ERR_INVALID;
+  ra::expected_work(S, c, layout, causal, out);
+  return RA_OK;
+}
+
+ra_status ra_ring_forward(const void* q, const void* k, const void* v, ra_shape shp, int c,
+                          int layout, int causal, int mode, void* out, float* lse,
+                          void* workspace, size_t ws_bytes, ra_report* report,
+                          ra_stream_t stream) {
+  ra_status st = check_ring(shp, c, layout);
+  if (st != RA_OK) return st;
+  if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (report != nullptr && report->c != c) return RA_ERR_INVALID;
+  st = ra_ring_prepare(q, k, v, shp, c, layout, workspace, ws_bytes, stream);
+  if (st != RA_OK) return st;
+  st = ra_ring_attend(shp, c, layout, causal, mode, out, lse, workspace, ws_bytes,
+                      report != nullptr && report->per_rank_step != nullptr, stream);
+  if (st != RA_OK || report == nullptr) return st;
+
+  // Report: device counters, host schedule and derived quantities.
+  const int S = shp.Sq;
+  const int n = c > 0 ? S / c : 0;
+  std::vector<ra_work> wk(static_cast<size_t>(c) * c);
+  if (report->per_rank_step != nullptr) {
+    if (shp.B > 0 && S > 0) {
+      st = ra_ring_read_work(shp, c, layout, mode, workspace, ws_bytes, report->per_rank_step,
+                             stream);
+      if (st != RA_OK) return st;
+    } else {
+      std::memset(report->per_rank_step, 0, sizeof(ra_work) * c * c);
+    }
+  }
+  st = ra_device_error(stream);
+  if (st != RA_OK) return st;
+  if (report->schedule != nullptr) ra_schedule(c, report->schedule);
+  std::vector<ra_work> exp(static_cast<size_t>(c) * c);
+  double tot_pairs = 0, max_pairs = 0, tot_tiles = 0, max_tiles = 0;
+  if (n > 0) {
+    ra::expected_work(S, c, layout, causal, exp.data());
+    for (int i = 0; i < c; ++i) {
+      double pr = 0, tl = 0;
+      for (int t = 0; t < c; ++t) {
+        const ra_work& e = exp[static_cast<size_t>(i) * c + t];
+        pr += static_cast<double>(e.pairs);
+        tl += static_cast<double>(e.tiles_full + e.tiles_partial);
+      }
+      tot_pairs += pr;
+      tot_tiles += tl;
+      if (pr > max_pairs) max_pairs = pr;
+      if (tl > max_tiles) max_tiles = tl;
+    }
+  }
+  report->imbalance_pairs = tot_pairs > 0 ? max_pairs / (tot_pairs / c) : 1.0;
+  report->imbalance_tiles = tot_tiles > 0 ? max_tiles / (tot_tiles / c) : 1.0;
+  const uint64_t kvb = static_cast<uint64_t>(S) * shp.Hkv * shp.D * 2 *
+                       static_cast<uint64_t>(elem_bytes(shp.dtype)) * shp.B;
+  report->ring_kv_bytes = kvb;
+  report->ring_kv_bytes_sent = kvb / c * (c - 1);
+  report->algorithmic_flop = static_cast<uint64_t>(4.0 * shp.B * shp.Hq * shp.D * tot_pairs);
+  return RA_OK;
+}
+
+size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode) {
+  const size_t base = ra_ring_forward_workspace_size(shp, c, layout, mode);
+  if (base == 0) return 0;
+  const size_t eb = static_cast<size_t>(elem_bytes(shp.dtype));
+  const size_t S = static_cast<size_t>(shp.Sq), B = static_cast<size_t>(shp.B), D = shp.D;
+  return base + round_up(B * S * shp.Hq * D * eb) + 2 * round_up(B * S * shp.Hkv * D * eb) +
+         round_up(B * S * shp.Hq * D * eb) + round_up(B * shp.Hq * S * sizeof(float));
+}
+
+ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const void* v_host,
+                                 ra_shape shp, int c, int layout, int causal, int mode,
+                                 void* out_host, float* lse_host, void* workspace,
+                                 size_t ws_bytes, ra_stream_t stream) {
+  ra_status st = check_ring(shp, c, layout);
+  if (st != RA_OK) return st;
+  if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (shp.B == 0 || shp.Sq == 0) return RA_OK;
+  if (!q_host || !k_host || !v_host || !out_host) return RA_ERR_INVALID;
+  const size_t need = ra_ring_forward_hostio_workspace_size(shp, c, layout, mode);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      ws_bytes < need)
+    return RA_ERR_WORKSPACE;
+  const size_t base = ra_ring_forward_workspace_size(shp, c, layout, mode);
+  const size_t eb = static_cast<size_t>(elem_bytes(shp.dtype));
+  const size_t S = static_cast<size_t>(shp.Sq), B = static_cast<size_t>(shp.B), D = shp.D;
+  const size_t qb = B * S * shp.Hq * D * eb, kb = B * S * shp.Hkv * D * eb;
+  const size_t lb = B * shp.Hq * S * sizeof(float);
+  char* p = static_cast<char*>(workspace) + base;
+  void* dq = p;  p += round_up(qb);
+  void* dk = p;  p += round_up(kb);
+  void* dv = p;  p += round_up(kb);
+  void* dout = p; p += round_up(qb);
+  float* dlse = reinterpret_cast<float*>(p);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return RA_ERR_CUDA;
+  st = ra_ring_forward(dq, dk, dv, shp, c, layout, causal, mode, dout,
+                       lse_host ? dlse : nullptr, workspace, base, nullptr, stream);
+  if (st != RA_OK) return st;
+  if (cudaMemcpyAsync(out_host, dout, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return RA_ERR_CUDA;
+  if (lse_host && cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RA_ERR_CUDA;
+  return RA_OK;
+}
+
+}  // extern "C"

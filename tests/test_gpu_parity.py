@@ -1,0 +1,251 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Every test calls the library (``libra_gb300.so``) through its Python binding
+on seeded synthetic inputs and compares with the oracle computed on the CPU
+from the same (already rounded) inputs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import context_exact_attention_ra_gb300 as ra
+import oracle
+from oracle import ring
+from tests import parity
+from workloads import WORKLOADS, make_inputs, small_case
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    ra.lib()
+    yield
+    ra.device_error()
+
+
+def _np(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _run(w, layout, mode="fused", report=False):
+    q, k, v, offsets = make_inputs(w)
+    res = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, layout, w.causal, mode,
+                          scale=w.scale, report=report)
+    ra.device_error()
+    return (q, k, v, offsets), res
+
+
+def _oracle_rows(q, k, v, w, rows):
+    pos = np.arange(w.S)
+    ref, lse, _, _ = oracle.attention_reference(_np(q), _np(k), _np(v), pos, pos, w.causal,
+                                                w.scale, rows=rows)
+    return ref, lse
+
+
+# ---------------------------------------------------------------------------
+# Full-size parity on the small workloads
+# ---------------------------------------------------------------------------
+
+def test_tiny_fp32_exact_path():
+    w = WORKLOADS["tiny"]
+    (q, k, v, _), (out, lse) = _run(w, "contiguous")
+    ref, ref_lse = _oracle_rows(q, k, v, w, np.arange(w.S))
+    parity.check_f32(_np(out), ref, "tiny out")
+    fin = np.isfinite(ref_lse)
+    rel = np.abs(_np(lse)[fin] - ref_lse[fin]).max() / np.abs(ref_lse[fin]).max()
+    assert rel <= parity.F32_REL
+
+
+def test_gqa4k_full_parity_and_modes_agree_bitwise():
+    w = WORKLOADS["gqa4k"]
+    (q, k, v, _), (out, lse, info) = _run(w, "zigzag", "fused", report=True)
+    ref, ref_lse = _oracle_rows(q, k, v, w, np.arange(w.S))
+    parity.check_bf16(_np(out), ref, "gqa4k out")
+    parity.check_lse(_np(lse), ref_lse, "gqa4k lse")
+    out2, lse2 = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, "per_step",
+                                 scale=w.scale)
+    ra.device_error()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+
+
+@pytest.mark.parametrize("name,layout", [("gqa4k", "zigzag"), ("s32k", "contiguous"),
+                                         ("s32k", "zigzag"), ("tiny", "contiguous")])
+def test_work_counters_match_host_scheduler_and_oracle(name, layout):
+    w = WORKLOADS[name]
+    _, (_, _, info) = _run(w, layout, "fused", report=True)
+    exp = ra.work_expected(w.S, w.c, layout, w.causal)
+    orc = ring.work_table(w.S, w.c, layout, w.causal)
+    scale = w.B * w.Hq
+    for i in range(w.c):
+        for t in range(w.c):
+            got = info["per_rank_step"][i][t]
+            e = exp[i][t]
+            assert (got["pairs"], got["full"], got["partial"], got["skipped"]) == \
+                tuple(x * scale for x in e), (i, t)
+            assert e == (orc["pairs"][i, t], orc["full"][i, t], orc["partial"][i, t],
+                         orc["skipped"][i, t])
+    assert info["schedule"] == ring.schedule(w.c)
+    per_rank = [sum(info["per_rank_step"][i][t]["pairs"] for t in range(w.c)) for i in range(w.c)]
+    if layout == "zigzag":
+        assert len(set(per_rank)) == 1
+    assert info["ring_kv_bytes"] == ring.ring_kv_bytes(w.S, w.Hkv, w.D, 2 if w.dtype == "bf16" else 4, w.B)
+
+
+# ---------------------------------------------------------------------------
+# Sampled-row parity on the large workloads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,layout", [("s32k", "contiguous"), ("s32k", "zigzag"),
+                                         ("s128k", "zigzag"), ("stress", "zigzag")])
+def test_large_workloads_sampled_rows(name, layout):
+    w = WORKLOADS[name]
+    (q, k, v, offsets), (out, lse) = _run(w, layout)
+    extra = []
+    for rows in offsets.values():
+        extra.extend(rows.tolist())
+    rows = parity.sample_rows(w.S, w.c, layout, w.seed, extra=extra[:64])
+    ref, ref_lse = _oracle_rows(q, k, v, w, rows)
+    got = _np(out[:, torch.as_tensor(rows)])
+    parity.check_bf16(got, ref, f"{name}/{layout} out")
+    parity.check_lse(_np(lse[:, :, torch.as_tensor(rows)]), ref_lse, f"{name}/{layout} lse")
+    # properties that hold for every row: finite, and |out| bounded by max |v|
+    o = out.float()
+    assert torch.isfinite(o).all()
+    assert o.abs().max().item() <= v.float().abs().max().item() * (1 + 1e-2) + 1e-2
+    assert torch.isfinite(lse).all()
+
+
+# ---------------------------------------------------------------------------
+# Edge cases: ragged shards, D=64, batch > 1, c = 1, tiny chunks
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S,c,layout,causal,B,Hq,Hkv,D,dtype", [
+    (1000, 5, "zigzag", True, 1, 4, 2, 128, "bf16"),        # chunks of 100 rows
+    (600, 2, "contiguous", False, 2, 2, 1, 128, "bf16"),    # shards of 300 rows
+    (768, 3, "contiguous", True, 1, 4, 4, 64, "bf16"),      # D = 64, MHA
+    (512, 1, "contiguous", True, 2, 8, 1, 128, "bf16"),     # one rank
+    (256, 64, "zigzag", True, 1, 2, 1, 128, "bf16"),        # chunks of 2 rows
+    (384, 3, "zigzag", True, 1, 2, 1, 128, "f32"),          # fp32, D = 128, ragged tiles
+    (200, 4, "contiguous", True, 2, 4, 2, 64, "f32"),
+])
+def test_edge_cases_full_parity(S, c, layout, causal, B, Hq, Hkv, D, dtype):
+    w = small_case(S, c, layout, causal, B=B, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, seed=S + c)
+    (q, k, v, _), (out, lse, info) = _run(w, layout, "fused", report=True)
+    ref, ref_lse = _oracle_rows(q, k, v, w, np.arange(S))
+    if dtype == "bf16":
+        parity.check_bf16(_np(out), ref, "edge out")
+        parity.check_lse(_np(lse), ref_lse, "edge lse")
+    else:
+        parity.check_f32(_np(out), ref, "edge out")
+    out2, lse2 = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), c, layout, causal, "per_step",
+                                 scale=w.scale)
+    ra.device_error()
+    assert torch.equal(out.view(torch.uint8), out2.view(torch.uint8))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    exp = ra.work_expected(S, c, layout, causal)
+    for i in range(c):
+        for t in range(c):
+            got = info["per_rank_step"][i][t]
+            assert (got["pairs"], got["full"], got["partial"], got["skipped"]) == \
+                tuple(x * B * Hq for x in exp[i][t])
+
+
+def test_empty_sequence_is_a_noop():
+    q = torch.empty((1, 0, 2, 128), dtype=torch.bfloat16, device=DEV)
+    k = torch.empty((1, 0, 1, 128), dtype=torch.bfloat16, device=DEV)
+    out, lse = ra.ring_forward(q, k, k, 2, "zigzag", True, "fused", workspace=torch.empty(256, dtype=torch.uint8, device=DEV))
+    assert out.numel() == 0 and lse.numel() == 0
+
+
+# ---------------------------------------------------------------------------
+# ra_block_attn and ra_lse_merge on their own
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_block_attn_arbitrary_positions_and_state(dtype):
+    # one rank's queries against two held blocks, positions scrambled
+    rng = np.random.default_rng(3)
+    B, Sq, Sk, Hq, Hkv, D = 2, 300, 260, 4, 2, 128
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn((B, Sq, Hq, D), generator=g).to(tdt)
+    k1 = torch.randn((B, Sk, Hkv, D), generator=g).to(tdt)
+    v1 = torch.randn((B, Sk, Hkv, D), generator=g).to(tdt)
+    k2 = torch.randn((B, Sk, Hkv, D), generator=g).to(tdt)
+    v2 = torch.randn((B, Sk, Hkv, D), generator=g).to(tdt)
+    perm = rng.permutation(2000)
+    qp, kp1, kp2 = perm[:Sq], perm[Sq:Sq + Sk], perm[Sq + Sk:Sq + 2 * Sk]
+    scale = D ** -0.5
+    o, m, l = ra.state_init(B, Sq, Hq, D)
+    work = torch.zeros(4, dtype=torch.int64, device=DEV)
+    for kk, vv, kp in ((k1, v1, kp1), (k2, v2, kp2)):
+        ra.block_attn(q.to(DEV), kk.to(DEV), vv.to(DEV), torch.as_tensor(qp, dtype=torch.int32, device=DEV),
+                      torch.as_tensor(kp, dtype=torch.int32, device=DEV), True, o, m, l, scale=scale,
+                      work=work)
+    ra.device_error()
+    # the state after both blocks: compare with the oracle's partial over the union
+    K = torch.cat([k1, k2], 1)
+    V = torch.cat([v1, v2], 1)
+    kp = np.concatenate([kp1, kp2])
+    ob, mb, lb = ring.block_partial(_np(q), _np(K), _np(V), qp, kp, True, scale)
+    m_nat = _np(m) * np.log(2.0)
+    fin = np.isfinite(mb)
+    assert (np.isfinite(m_nat) == fin).all()
+    # state normalised by its own l equals the oracle's normalised output
+    out = _np(o) / np.where(_np(l) > 0, _np(l), 1.0).transpose(0, 2, 1)[..., None]
+    ref = ob / np.where(lb > 0, lb, 1.0).transpose(0, 2, 1)[..., None]
+    lse = np.where(_np(l) > 0, m_nat + np.log(np.where(_np(l) > 0, _np(l), 1.0)), -np.inf)
+    ref_lse = np.where(lb > 0, mb + np.log(np.where(lb > 0, lb, 1.0)), -np.inf)
+    if dtype == "bf16":
+        parity.check_bf16(out, ref, "block out")
+    else:
+        parity.check_f32(out, ref, "block out")
+    parity.check_lse(lse, ref_lse, "block lse")
+    pairs = ring.visible_pairs(qp, kp1, True) + ring.visible_pairs(qp, kp2, True)
+    assert int(work[0].item()) == pairs * B * Hq
+
+
+@pytest.mark.parametrize("P", [1, 3])
+def test_lse_merge_of_key_splits_equals_full_attention(P):
+    B, S, Hq, Hkv, D = 1, 512, 4, 1, 128
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn((B, S, Hq, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, S, Hkv, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, S, Hkv, D), generator=g).to(torch.bfloat16)
+    pos = torch.arange(S, dtype=torch.int32, device=DEV)
+    edges = np.linspace(0, S, P + 1).astype(int)
+    outs, ms, ls = [], [], []
+    for a, b in zip(edges[:-1], edges[1:]):
+        o, m, l = ra.state_init(B, S, Hq, D)
+        ra.block_attn(q.to(DEV), k[:, a:b].contiguous().to(DEV), v[:, a:b].contiguous().to(DEV),
+                      pos, pos[a:b].contiguous(), True, o, m, l)
+        outs.append(o)
+        ms.append(m)
+        ls.append(l)
+    out, lse = ra.lse_merge(outs, ms, ls, torch.bfloat16)
+    out32, _ = ra.lse_merge(outs, ms, ls, torch.float32)
+    ra.device_error()
+    ref, ref_lse, _, _ = oracle.attention_reference(_np(q), _np(k), _np(v), np.arange(S), np.arange(S),
+                                                    True, D ** -0.5)
+    parity.check_bf16(_np(out), ref, "merge out")
+    parity.check_bf16(_np(out32), ref, "merge out f32")
+    parity.check_lse(_np(lse), ref_lse, "merge lse")
+
+
+def test_hostio_equals_device_path():
+    w = small_case(2048, 4, "zigzag", True, B=1, Hq=4, Hkv=1, D=128, seed=21)
+    q, k, v, _ = make_inputs(w)
+    out_d, lse_d = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, "fused")
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    out_h = torch.empty_like(qh).pin_memory()
+    lse_h = torch.empty((1, w.Hq, w.S), dtype=torch.float32).pin_memory()
+    ra.ring_forward_hostio(qh, kh, vh, w.c, "zigzag", True, "fused", out_host=out_h, lse_host=lse_h)
+    assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
+    assert torch.equal(lse_h.view(torch.int32), lse_d.cpu().view(torch.int32))
