@@ -67,18 +67,18 @@ _SIGS = {
     "ra_lse_merge": (ctypes.c_int, [ctypes.c_int, _P, _P, _P, Shape, _P, _P, _P]),
     "ra_ring_forward_workspace_size": (ctypes.c_size_t, [Shape, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "ra_ring_forward": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                       ctypes.c_int, _P, _P, _P, ctypes.c_size_t,
+                                       ctypes.c_int, ctypes.c_int, _P, _P, _P, ctypes.c_size_t,
                                        ctypes.POINTER(Report), _P]),
     "ra_ring_prepare": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.c_int, ctypes.c_int, _P,
                                        ctypes.c_size_t, _P]),
     "ra_ring_attend": (ctypes.c_int, [Shape, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                      _P, _P, _P, ctypes.c_size_t, ctypes.c_int, _P]),
+                                      ctypes.c_int, _P, _P, _P, ctypes.c_size_t, ctypes.c_int, _P]),
     "ra_ring_read_work": (ctypes.c_int, [Shape, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P,
                                          ctypes.c_size_t, ctypes.POINTER(Work), _P]),
     "ra_ring_forward_hostio_workspace_size": (ctypes.c_size_t, [Shape, ctypes.c_int, ctypes.c_int,
-                                                                ctypes.c_int]),
+                                                                ctypes.c_int, ctypes.c_int]),
     "ra_ring_forward_hostio": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.c_int, ctypes.c_int,
-                                              ctypes.c_int, ctypes.c_int, _P, _P, _P,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P,
                                               ctypes.c_size_t, _P]),
     "ra_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int32)]),
     "ra_shard_positions": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -156,20 +156,27 @@ def ring_workspace_size(shape: Shape, c, layout, mode):
     return int(lib().ra_ring_forward_workspace_size(shape, int(c), int(layout), int(mode)))
 
 
+def _out_code(out_dtype, q):
+    dt = q.dtype if out_dtype is None else out_dtype
+    return _dtype_code(torch.empty(0, dtype=dt)), dt
+
+
 def ring_forward(q, k, v, c, layout="zigzag", causal=True, mode="fused", scale=None,
-                 workspace=None, report=False, stream=None):
+                 workspace=None, report=False, stream=None, out_dtype=None):
     """Ring attention of q [B,S,Hq,D] over k, v [B,S,Hkv,D] with c virtual ranks.
 
-    Returns (out [B,S,Hq,D] in q's dtype, lse [B,Hq,S] float32) and, with
-    ``report=True``, a dict of per-(rank, step) work counted on the GPU, the
-    ring schedule and the derived quantities.
+    Returns (out [B,S,Hq,D] in out_dtype (default q's dtype; torch.float32
+    gives the result before its rounding to bf16), lse [B,Hq,S] float32) and,
+    with ``report=True``, a dict of per-(rank, step) work counted on the GPU,
+    the ring schedule and the derived quantities.
     """
     _contig(q, k, v)
     lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     md = MODES[mode] if isinstance(mode, str) else int(mode)
     scale = q.shape[-1] ** -0.5 if scale is None else scale
     shp = _shape(q, k, scale)
-    out = torch.empty_like(q)
+    ocode, odt = _out_code(out_dtype, q)
+    out = torch.empty(q.shape, dtype=odt, device=q.device)
     lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
     need = ring_workspace_size(shp, c, lay, md)
     if need == 0 and q.numel() > 0:
@@ -185,7 +192,7 @@ def ring_forward(q, k, v, c, layout="zigzag", causal=True, mode="fused", scale=N
         rep = Report(c, ctypes.cast(work, ctypes.POINTER(Work)),
                      ctypes.cast(sched, ctypes.POINTER(ctypes.c_int32)), 0, 0, 0, 0, 0)
     st = lib().ra_ring_forward(_ptr(q), _ptr(k), _ptr(v), shp, int(c), lay, int(bool(causal)), md,
-                               _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                               ocode, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                ctypes.byref(rep) if rep is not None else None, _stream(stream))
     _check(st, "ra_ring_forward")
     if not report:
@@ -217,7 +224,8 @@ def ring_attend(shape: Shape, c, layout, causal, mode, out, lse, workspace, coun
                 stream=None):
     lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     md = MODES[mode] if isinstance(mode, str) else int(mode)
-    st = lib().ra_ring_attend(shape, int(c), lay, int(bool(causal)), md, _ptr(out), _ptr(lse),
+    st = lib().ra_ring_attend(shape, int(c), lay, int(bool(causal)), md, _dtype_code(out),
+                              _ptr(out), _ptr(lse),
                               _ptr(workspace), workspace.numel(), int(bool(count_work)),
                               _stream(stream))
     _check(st, "ra_ring_attend")
@@ -244,18 +252,20 @@ def ring_forward_hostio(q_host, k_host, v_host, c, layout="zigzag", causal=True,
     shp = _shape(q_host, k_host, scale)
     if out_host is None:
         out_host = torch.empty_like(q_host)
-    need = int(lib().ra_ring_forward_hostio_workspace_size(shp, int(c), lay, md))
+    ocode = _dtype_code(out_host)
+    need = int(lib().ra_ring_forward_hostio_workspace_size(shp, int(c), lay, md, ocode))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
     st = lib().ra_ring_forward_hostio(_ptr(q_host), _ptr(k_host), _ptr(v_host), shp, int(c), lay,
-                                      int(bool(causal)), md, _ptr(out_host), _ptr(lse_host),
+                                      int(bool(causal)), md, ocode, _ptr(out_host), _ptr(lse_host),
                                       _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "ra_ring_forward_hostio")
     return out_host, lse_host
 
 
-def hostio_workspace_size(shape: Shape, c, layout, mode):
-    return int(lib().ra_ring_forward_hostio_workspace_size(shape, int(c), int(layout), int(mode)))
+def hostio_workspace_size(shape: Shape, c, layout, mode, out_dtype_code=None):
+    oc = shape.dtype if out_dtype_code is None else out_dtype_code
+    return int(lib().ra_ring_forward_hostio_workspace_size(shape, int(c), int(layout), int(mode), oc))
 
 
 def state_init(B, S, Hq, D, device="cuda", dtype_code=BF16, stream=None):

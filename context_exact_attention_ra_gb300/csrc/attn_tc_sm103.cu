@@ -79,7 +79,9 @@ struct Smem {
   static constexpr int bDrain = bOFinal + 1;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kRange = kMisc + 16;          // (min, max) key position per key tile
+  static constexpr int kMaxRanges = 2048;
+  static constexpr int kBytes = kRange + kMaxRanges * 8;
   static constexpr int kDynamic = kBytes + 1024;     // room to align the base to 1024
   static_assert(kDynamic <= 232448, "shared memory budget");
 };
@@ -98,7 +100,7 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, Abort 
   const uint64_t t0 = ptx::global_timer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 4; ++i)
       if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*ab.flag) return false;
     if (*reinterpret_cast<volatile unsigned int*>(ab.err) != 0) {
@@ -171,12 +173,21 @@ struct KTile {
   bool skip;   // hidden from both query tiles
 };
 
+// Key tile kt of shard `src`.  `rs` holds the (min, max) positions of the
+// tiles of this step in shared memory, or is null (then they are reduced
+// from the positions by the calling warp).
 __device__ __forceinline__ KTile k_tile(const AttnParams& p, int src, int kt, const QTiles& q,
-                                        int lane) {
+                                        int lane, const int2* rs) {
   KTile k;
   const int start = kt * kTile;
   k.valid = min(kTile, p.n_k - start);
-  warp_minmax(p.k_pos + static_cast<long long>(src) * p.n_k + start, k.valid, lane, k.mn, k.mx);
+  if (rs != nullptr) {
+    const int2 r = rs[kt];
+    k.mn = r.x;
+    k.mx = r.y;
+  } else {
+    warp_minmax(p.k_pos + static_cast<long long>(src) * p.n_k + start, k.valid, lane, k.mn, k.mx);
+  }
   k.skip = p.causal ? (k.mn > q.mx_all) : (q.valid[0] + q.valid[1] == 0);
   return k;
 }
@@ -187,7 +198,7 @@ __device__ __forceinline__ int ring_src(int rank, int t, int c) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(184)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -245,6 +256,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
   }
+  // Stage the (min, max) key position of every key tile this block visits.
+  int2* const ranges = reinterpret_cast<int2*>(smem + L::kRange);
+  const int nsteps = p.t_end - p.t_begin;
+  const bool staged = static_cast<long long>(nsteps) * ktiles <= L::kMaxRanges;
+  if (staged) {
+    const int total = nsteps * ktiles;
+    if (p.k_ranges != nullptr) {
+      for (int i = threadIdx.x; i < total; i += kThreads) {
+        const int src = ring_src(rank, p.t_begin + i / ktiles, p.c);
+        ranges[i] = p.k_ranges[static_cast<long long>(src) * ktiles + i % ktiles];
+      }
+    } else {
+      for (int i = warp; i < total; i += kThreads / 32) {
+        const int src = ring_src(rank, p.t_begin + i / ktiles, p.c);
+        const int kt = i % ktiles;
+        int mn, mx;
+        warp_minmax(p.k_pos + static_cast<long long>(src) * p.n_k + kt * kTile,
+                    min(kTile, p.n_k - kt * kTile), lane, mn, mx);
+        if (lane == 0) ranges[i] = make_int2(mn, mx);
+      }
+    }
+  }
+  auto step_ranges = [&](int t) -> const int2* {
+    return staged ? ranges + (t - p.t_begin) * ktiles : nullptr;
+  };
   ptx::tc_fence_before_sync();
   __syncthreads();
   ptx::tc_fence_after_sync();
@@ -272,8 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = !*abort_flag;
     for (int t = p.t_begin; t < p.t_end && ok; ++t) {
       const int src = ring_src(rank, t, p.c);
+      const int2* rs = step_ranges(t);
       for (int kt = 0; kt < ktiles; ++kt) {
-        const KTile k = k_tile(p, src, kt, qt, lane);
+        const KTile k = k_tile(p, src, kt, qt, lane, rs);
         if (k.skip) continue;
         if (lane == 0) {
           const int s = static_cast<int>(j % nst);
@@ -331,9 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t j = 0;
     for (int t = p.t_begin; t < p.t_end && ok; ++t) {
       const int src = ring_src(rank, t, p.c);
+      const int2* rs = step_ranges(t);
       unsigned long long nfull = 0, npart = 0, nskip = 0;
       for (int kt = 0; kt < ktiles; ++kt) {
-        const KTile k = k_tile(p, src, kt, qt, lane);
+        const KTile k = k_tile(p, src, kt, qt, lane, rs);
         if (p.work != nullptr) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
@@ -453,10 +491,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = p.t_begin; t < p.t_end && ok; ++t) {
       const int src = ring_src(rank, t, p.c);
+      const int2* rs = step_ranges(t);
       const int32_t* kpos_src = p.k_pos + static_cast<long long>(src) * p.n_k;
       unsigned long long pairs = 0;
       for (int kt = 0; kt < ktiles; ++kt) {
-        const KTile k = k_tile(p, src, kt, qt, lane);
+        const KTile k = k_tile(p, src, kt, qt, lane, rs);
         if (k.skip) continue;
         ok = __all_sync(0xffffffffu, wait_bar(bar(L::bSFull + hh), j & 1u, ab, kErrTimeoutS));
         if (!ok) break;
@@ -464,52 +503,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool masked = (k.valid < kTile) || (p.causal && k.mx > qt.mn[hh]);
         const int32_t* kp = kpos_src + kt * kTile;
 
-        // pass 1: row maximum of the visible scores
-        float mx = -INFINITY;
+        // visibility of each key column (partial tiles only), before S is loaded
+        uint32_t bits[4] = {~0u, ~0u, ~0u, ~0u};
+        unsigned int nvis = static_cast<unsigned int>(k.valid);
+        if (masked) {
+          nvis = 0;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t u[32];
-          ptx::tmem_ld32(tS + cc * 32, u);
-          if (masked) {
-#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t bb = 0;
+#pragma unroll 8
             for (int i = 0; i < 32; ++i) {
               const int col = cc * 32 + i;
               const bool vis = col < k.valid && (!p.causal || __ldg(kp + min(col, k.valid - 1)) <= qpos);
-              if (vis) mx = fmaxf(mx, __uint_as_float(u[i]));
+              bb |= (vis ? 1u : 0u) << i;
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(u[i]));
+            bits[cc] = bb;
+            nvis += __popc(bb);
           }
         }
+        uint32_t sv[128];
+        ptx::tmem_ld128(tS, sv);
+        if (masked) {
+          // hidden or padding keys become -inf before the max and the exponent
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (!((bits[i >> 5] >> (i & 31)) & 1u)) sv[i] = 0xff800000u;
+        }
+        // row maximum (four independent chains)
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; i += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sv[i]));
+          mx1 = fmaxf(mx1, __uint_as_float(sv[i + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sv[i + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sv[i + 3]));
+        }
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const float m_new = fmaxf(m_run, mx * sl2);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
-        // pass 2: probabilities, their sum, and P (bf16) over S's columns
-        float sum = 0.f;
-        unsigned int nvis = 0;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t u[32];
-          ptx::tmem_ld32(tS + cc * 32, u);
-          float pr[32];
+        // probabilities, their sum, and P (bf16) over the first 64 columns of S
+        float sm0 = 0.f, sm1 = 0.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float e = ptx::ex2(fmaf(__uint_as_float(u[i]), sl2, -m_use));
-            bool vis = true;
-            if (masked) {
-              const int col = cc * 32 + i;
-              vis = col < k.valid && (!p.causal || __ldg(kp + min(col, k.valid - 1)) <= qpos);
-            }
-            pr[i] = vis ? e : 0.f;
-            nvis += vis ? 1u : 0u;
-            sum += pr[i];
-          }
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+          for (int i = 0; i < 16; ++i) {
+            const float e0 = ptx::ex2(fmaf(__uint_as_float(sv[cc * 32 + 2 * i]), sl2, -m_use));
+            const float e1 = ptx::ex2(fmaf(__uint_as_float(sv[cc * 32 + 2 * i + 1]), sl2, -m_use));
+            sm0 += e0;
+            sm1 += e1;
+            pk[i] = ptx::pack_bf16x2(e0, e1);
+          }
           ptx::tmem_st16(tS + cc * 16, pk);
         }
+        const float sum = sm0 + sm1;
         const float alpha = (m_run == m_new) ? 1.f : ptx::ex2(m_run - m_new);
         l_run = l_run * alpha + sum;
         // rescale the accumulator when the running maximum rose
@@ -548,14 +596,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.finalize) {
         const int orow = row_ok ? qpos : 0;
         const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                             ((static_cast<long long>(b) * p.S_out + orow) * p.Hq + h) * D;
+        const long long obase = ((static_cast<long long>(b) * p.S_out + orow) * p.Hq + h) * D;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t u[32];
           ptx::tmem_ld32(tO + cc * 32, u);
-          if (row_ok) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+          if (row_ok && p.out_f32) {
+            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(u[4 * i]) * inv_l, __uint_as_float(u[4 * i + 1]) * inv_l,
+                                  __uint_as_float(u[4 * i + 2]) * inv_l, __uint_as_float(u[4 * i + 3]) * inv_l);
+          } else if (row_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               uint4 w;

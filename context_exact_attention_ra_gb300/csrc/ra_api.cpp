@@ -51,6 +51,12 @@ ra_status check_ring(const ra_shape& s, int c, int layout) {
   return RA_OK;
 }
 
+// Output element type: the input dtype, or float32 (the fp32 result before
+// rounding; for f32 inputs the two coincide).
+bool out_dtype_ok(const ra_shape& s, int out_dtype) {
+  return out_dtype == s.dtype || out_dtype == RA_F32;
+}
+
 int rows_per_block(int dtype) { return dtype == RA_BF16 ? ra::kPairRows : ra::kTile; }
 
 int blocks_per_rank(const ra_shape& s, int n_q) {
@@ -60,7 +66,7 @@ int blocks_per_rank(const ra_shape& s, int n_q) {
 
 // Regions of a ring workspace, as byte offsets from its base.
 struct RingWs {
-  size_t qp, kp, vp, pos, order, work, o, m, l, total;
+  size_t qp, kp, vp, pos, ranges, order, work, o, m, l, total;
 };
 
 RingWs ring_ws(const ra_shape& s, int c, int mode) {
@@ -75,6 +81,8 @@ RingWs ring_ws(const ra_shape& s, int c, int mode) {
   w.kp = off;    off = round_up(off + B * S * s.Hkv * D * eb);
   w.vp = off;    off = round_up(off + B * S * s.Hkv * D * eb);
   w.pos = off;   off = round_up(off + S * sizeof(int32_t));
+  w.ranges = off;
+  off = round_up(off + static_cast<size_t>(c) * ((n + ra::kTile - 1) / ra::kTile) * 2 * sizeof(int32_t));
   w.order = off; off = round_up(off + nblocks * sizeof(int32_t));
   w.work = off;  off = round_up(off + static_cast<size_t>(c) * c * sizeof(ra_work));
   if (mode == RA_MODE_PER_STEP) {
@@ -217,8 +225,11 @@ ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape 
                           c, layout, at<void>(workspace, w.qp), at<void>(workspace, w.kp),
                           at<void>(workspace, w.vp), at<int32_t>(workspace, w.pos), stream);
   if (e) return RA_ERR_CUDA;
-  // Heavy-first block order (used by causal calls): depends on positions only.
   const int n = shp.Sq / c;
+  e = ra::launch_tile_ranges(at<int32_t>(workspace, w.pos), c, n, at<int2>(workspace, w.ranges),
+                             stream);
+  if (e) return RA_ERR_CUDA;
+  // Heavy-first block order (used by causal calls): depends on positions only.
   const int total_blocks = c * blocks_per_rank(shp, n);
   if (total_blocks > 1 && total_blocks <= ra::kMaxOrderedBlocks) {
     e = ra::launch_block_order(at<int32_t>(workspace, w.pos), c, n, rows_per_block(shp.dtype),
@@ -228,12 +239,13 @@ ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape 
   return RA_OK;
 }
 
-ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, void* out,
-                         float* lse, void* workspace, size_t ws_bytes, int count_work,
+ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, int out_dtype,
+                         void* out, float* lse, void* workspace, size_t ws_bytes, int count_work,
                          ra_stream_t stream) {
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
   if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (!out_dtype_ok(shp, out_dtype)) return RA_ERR_INVALID;
   if (shp.B == 0 || shp.Sq == 0) return RA_OK;
   if (out == nullptr || !aligned16(out)) return RA_ERR_INVALID;
   const RingWs w = ring_ws(shp, c, mode);
@@ -249,11 +261,13 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
   AttnParams p = base_params(shp, c, n, n, causal);
   p.q_pos = at<int32_t>(workspace, w.pos);
   p.k_pos = p.q_pos;
+  p.k_ranges = at<int2>(workspace, w.ranges);
   p.q = at<void>(workspace, w.qp);
   p.k = at<void>(workspace, w.kp);
   p.v = at<void>(workspace, w.vp);
   p.err = ew;
   p.out = out;
+  p.out_f32 = (out_dtype == RA_F32) ? 1 : 0;
   p.lse = lse;
   p.S_out = S;
   if (count_work) {
@@ -291,7 +305,7 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
   a.outs[0] = p.o_state;
   a.ms[0] = p.m_state;
   a.ls[0] = p.l_state;
-  return cuda_status(ra::launch_merge(a, shp.B, S, shp.Hq, shp.D, shp.dtype, out, lse, p.q_pos, S,
+  return cuda_status(ra::launch_merge(a, shp.B, S, shp.Hq, shp.D, out_dtype, out, lse, p.q_pos, S,
                                       stream));
 }
 
@@ -343,16 +357,17 @@ ra_status ra_work_expected(int S, int c, int layout, int causal, ra_work* out) {
 }
 
 ra_status ra_ring_forward(const void* q, const void* k, const void* v, ra_shape shp, int c,
-                          int layout, int causal, int mode, void* out, float* lse,
+                          int layout, int causal, int mode, int out_dtype, void* out, float* lse,
                           void* workspace, size_t ws_bytes, ra_report* report,
                           ra_stream_t stream) {
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
   if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (!out_dtype_ok(shp, out_dtype)) return RA_ERR_INVALID;
   if (report != nullptr && report->c != c) return RA_ERR_INVALID;
   st = ra_ring_prepare(q, k, v, shp, c, layout, workspace, ws_bytes, stream);
   if (st != RA_OK) return st;
-  st = ra_ring_attend(shp, c, layout, causal, mode, out, lse, workspace, ws_bytes,
+  st = ra_ring_attend(shp, c, layout, causal, mode, out_dtype, out, lse, workspace, ws_bytes,
                       report != nullptr && report->per_rank_step != nullptr, stream);
   if (st != RA_OK || report == nullptr) return st;
 
@@ -399,25 +414,28 @@ ra_status ra_ring_forward(const void* q, const void* k, const void* v, ra_shape 
   return RA_OK;
 }
 
-size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode) {
+size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode,
+                                             int out_dtype) {
   const size_t base = ra_ring_forward_workspace_size(shp, c, layout, mode);
-  if (base == 0) return 0;
+  if (base == 0 || !out_dtype_ok(shp, out_dtype)) return 0;
   const size_t eb = static_cast<size_t>(elem_bytes(shp.dtype));
+  const size_t ob = static_cast<size_t>(elem_bytes(out_dtype));
   const size_t S = static_cast<size_t>(shp.Sq), B = static_cast<size_t>(shp.B), D = shp.D;
   return base + round_up(B * S * shp.Hq * D * eb) + 2 * round_up(B * S * shp.Hkv * D * eb) +
-         round_up(B * S * shp.Hq * D * eb) + round_up(B * shp.Hq * S * sizeof(float));
+         round_up(B * S * shp.Hq * D * ob) + round_up(B * shp.Hq * S * sizeof(float));
 }
 
 ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const void* v_host,
                                  ra_shape shp, int c, int layout, int causal, int mode,
-                                 void* out_host, float* lse_host, void* workspace,
+                                 int out_dtype, void* out_host, float* lse_host, void* workspace,
                                  size_t ws_bytes, ra_stream_t stream) {
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
   if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (!out_dtype_ok(shp, out_dtype)) return RA_ERR_INVALID;
   if (shp.B == 0 || shp.Sq == 0) return RA_OK;
   if (!q_host || !k_host || !v_host || !out_host) return RA_ERR_INVALID;
-  const size_t need = ra_ring_forward_hostio_workspace_size(shp, c, layout, mode);
+  const size_t need = ra_ring_forward_hostio_workspace_size(shp, c, layout, mode, out_dtype);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       ws_bytes < need)
     return RA_ERR_WORKSPACE;
@@ -425,22 +443,23 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
   const size_t eb = static_cast<size_t>(elem_bytes(shp.dtype));
   const size_t S = static_cast<size_t>(shp.Sq), B = static_cast<size_t>(shp.B), D = shp.D;
   const size_t qb = B * S * shp.Hq * D * eb, kb = B * S * shp.Hkv * D * eb;
+  const size_t ob = B * S * shp.Hq * D * static_cast<size_t>(elem_bytes(out_dtype));
   const size_t lb = B * shp.Hq * S * sizeof(float);
   char* p = static_cast<char*>(workspace) + base;
   void* dq = p;  p += round_up(qb);
   void* dk = p;  p += round_up(kb);
   void* dv = p;  p += round_up(kb);
-  void* dout = p; p += round_up(qb);
+  void* dout = p; p += round_up(ob);
   float* dlse = reinterpret_cast<float*>(p);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return RA_ERR_CUDA;
-  st = ra_ring_forward(dq, dk, dv, shp, c, layout, causal, mode, dout,
+  st = ra_ring_forward(dq, dk, dv, shp, c, layout, causal, mode, out_dtype, dout,
                        lse_host ? dlse : nullptr, workspace, base, nullptr, stream);
   if (st != RA_OK) return st;
-  if (cudaMemcpyAsync(out_host, dout, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return RA_ERR_CUDA;
+  if (cudaMemcpyAsync(out_host, dout, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess) return RA_ERR_CUDA;
   if (lse_host && cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return RA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return RA_ERR_CUDA;

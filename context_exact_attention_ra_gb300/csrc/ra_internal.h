@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <vector_types.h>
+
 #include "ra.h"
 
 namespace ra {
@@ -29,6 +31,7 @@ struct AttnParams {
 
   const int32_t* q_pos;        // [c*n_q]
   const int32_t* k_pos;        // [c*n_k]
+  const int2* k_ranges;        // [c*ceil(n_k/128)] (min, max) position per key tile, or nullptr
 
   const void* q;               // [B, c*n_q, Hq, D]   (fp32 kernel; bf16 uses tensor maps)
   const void* k;               // [B, c*n_k, Hkv, D]
@@ -42,7 +45,8 @@ struct AttnParams {
   int store_state;             // write (o, m, l) after the last step
   // normalised output (finalize): row = q_pos[q row] of an S_out-row tensor
   int finalize;
-  void* out;                   // [B, S_out, Hq, D] in the input dtype
+  int out_f32;                 // output element type: 1 = float32, 0 = the input dtype
+  void* out;                   // [B, S_out, Hq, D]
   float* lse;                  // [B, Hq, S_out] or nullptr
   int S_out;
 
@@ -71,6 +75,7 @@ int launch_state_init(int B, int rows, int Hq, int D, float* o, float* m, float*
 int launch_pack(const void* q, const void* k, const void* v, int B, int S, int Hq, int Hkv,
                 int D, int elem_bytes, int c, int layout, void* qp, void* kp, void* vp,
                 int32_t* pos, void* stream);
+int launch_tile_ranges(const int32_t* pos, int c, int n, int2* ranges, void* stream);
 int launch_block_order(const int32_t* pos, int c, int n, int rows_per_block,
                        int blocks_per_rank, int32_t* order, void* stream);
 struct MergeArgs {

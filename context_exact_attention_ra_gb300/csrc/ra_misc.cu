@@ -91,6 +91,29 @@ __global__ void block_order_kernel(const int32_t* pos, int c, int n, int rows_pe
   }
 }
 
+// One warp per 128-row tile of each shard: smallest and largest position.
+__global__ void tile_range_kernel(const int32_t* pos, int c, int n, int tiles, int2* out) {
+  const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp_id >= static_cast<long long>(c) * tiles) return;
+  const int r = static_cast<int>(warp_id / tiles);
+  const int t = static_cast<int>(warp_id % tiles);
+  const int a = t * kTile;
+  const int e = min(n, a + kTile);
+  int mn = INT_MAX, mx = INT_MIN;
+  for (int i = a + lane; i < e; i += 32) {
+    const int v = pos[static_cast<long long>(r) * n + i];
+    mn = min(mn, v);
+    mx = max(mx, v);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) out[warp_id] = make_int2(mn, mx);
+}
+
 struct MergeParams {
   MergeArgs a;
   int B, S, Hq, D, out_dtype, S_out;
@@ -204,6 +227,15 @@ int launch_pack(const void* q, const void* k, const void* v, int B, int S, int H
       static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v), S,
       n, c, layout, q_vec, kv_vec, static_cast<uint4*>(qp), static_cast<uint4*>(kp),
       static_cast<uint4*>(vp), pos);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_tile_ranges(const int32_t* pos, int c, int n, int2* ranges, void* stream) {
+  const int tiles = (n + kTile - 1) / kTile;
+  const long long warps = static_cast<long long>(c) * tiles;
+  if (warps == 0) return 0;
+  tile_range_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0,
+                      static_cast<cudaStream_t>(stream)>>>(pos, c, n, tiles, ranges);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -173,7 +173,10 @@ size_t ra_ring_forward_workspace_size(ra_shape shp, int c, int layout, int mode)
  * ra_ring_prepare followed by ra_ring_attend.
  *   q, k, v    device, natural token order, [B, S, Hq|Hkv, D] in shp.dtype
  *   c          ranks, 1 <= c; S % c == 0 (contiguous) or S % (2c) == 0 (zig-zag)
- *   out        device [B, S, Hq, D] in shp.dtype, natural order
+ *   out_dtype  element type of out: shp.dtype, or RA_F32 to receive the
+ *              float32 result before its rounding to bf16 (the bf16 output is
+ *              exactly that result rounded to nearest even)
+ *   out        device [B, S, Hq, D] in out_dtype, natural order
  *   lse        device [B, Hq, S] float32 natural log, or NULL
  *   workspace  device, >= ra_ring_forward_workspace_size(...) bytes
  *   report     host, or NULL.  When non-NULL the call synchronises the
@@ -181,7 +184,7 @@ size_t ra_ring_forward_workspace_size(ra_shape shp, int c, int layout, int mode)
  *              and derived quantities from the host scheduler) and returns
  *              RA_ERR_TIMEOUT if a device wait ran out. */
 ra_status ra_ring_forward(const void* q, const void* k, const void* v, ra_shape shp,
-                          int c, int layout, int causal, int mode,
+                          int c, int layout, int causal, int mode, int out_dtype,
                           void* out, float* lse, void* workspace, size_t ws_bytes,
                           ra_report* report, ra_stream_t stream);
 
@@ -197,7 +200,7 @@ ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape 
  * reading the shards ra_ring_prepare left in the same workspace.
  * count_work nonzero zeroes and fills the per-(rank, step) counters kept in
  * the workspace (read them with ra_ring_read_work). */
-ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode,
+ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, int out_dtype,
                          void* out, float* lse, void* workspace, size_t ws_bytes,
                          int count_work, ra_stream_t stream);
 
@@ -211,10 +214,11 @@ ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const voi
  * on `stream`; returns after the stream has finished.  The device buffers
  * for q, k, v, out and lse are carved from the workspace, whose size is
  * ra_ring_forward_hostio_workspace_size(). */
-size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode);
+size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode,
+                                             int out_dtype);
 ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const void* v_host,
                                  ra_shape shp, int c, int layout, int causal, int mode,
-                                 void* out_host, float* lse_host, void* workspace,
+                                 int out_dtype, void* out_host, float* lse_host, void* workspace,
                                  size_t ws_bytes, ra_stream_t stream);
 
 /* ---- host-side scheduler (no GPU needed) ------------------------------ */

@@ -1,7 +1,11 @@
 """Helpers shared by the GPU parity tests: row sampling and tolerance checks.
 
 Tolerances (floating point, stated by the task description of the target):
-bf16 outputs within max-abs 1e-2 and mean-abs 1e-3 of the oracle; LSE within
+bf16 outputs within max-abs 1e-2 and mean-abs 1e-3 of the oracle, applied to
+the computed (fp32) result; its final rounding to bf16 adds up to half a bf16
+ulp of the value (0.0156 for |out| in [4, 8)), more than 1e-2 on its own, so
+the rounded output is checked to be exactly the fp32 result rounded to
+nearest even instead (``check_rounding``); LSE within
 1e-3, read as |d| <= 1e-3 * max(1, |lse|) because the stress workload's LSE
 reaches O(1e3), where one fp32 ulp is 6e-5 and the fp32 accumulation of a
 128-term dot product of O(1e3) logits carries errors of that order; fp32
@@ -63,6 +67,14 @@ def check_lse(lse, ref, what=""):
     bound = LSE_TOL * np.maximum(1.0, np.abs(ref[fin]))
     assert (d <= bound).all(), f"{what}: lse max {d.max():.3e} (worst ratio {(d / bound).max():.3f})"
     return float(d.max()) if d.size else 0.0
+
+
+def check_rounding(out_bf16, out_f32, what=""):
+    """The bf16 output is the fp32 result rounded to nearest even, bit for bit."""
+    import torch
+    want = out_f32.to(torch.bfloat16)
+    same = torch.equal(out_bf16.view(torch.int16), want.view(torch.int16))
+    assert same, f"{what}: bf16 output is not the rounded fp32 result"
 
 
 def check_f32(out, ref, what=""):

@@ -33,10 +33,10 @@ def _np(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def _run(w, layout, mode="fused", report=False):
+def _run(w, layout, mode="fused", report=False, out_dtype=None):
     q, k, v, offsets = make_inputs(w)
     res = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, layout, w.causal, mode,
-                          scale=w.scale, report=report)
+                          scale=w.scale, report=report, out_dtype=out_dtype)
     ra.device_error()
     return (q, k, v, offsets), res
 
@@ -68,11 +68,18 @@ def test_gqa4k_full_parity_and_modes_agree_bitwise():
     ref, ref_lse = _oracle_rows(q, k, v, w, np.arange(w.S))
     parity.check_bf16(_np(out), ref, "gqa4k out")
     parity.check_lse(_np(lse), ref_lse, "gqa4k lse")
+    out32, _ = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, "fused",
+                               scale=w.scale, out_dtype=torch.float32)
+    parity.check_bf16(_np(out32), ref, "gqa4k out fp32")
+    parity.check_rounding(out, out32, "gqa4k")
     out2, lse2 = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, "per_step",
                                  scale=w.scale)
+    out2_32, _ = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, "per_step",
+                                 scale=w.scale, out_dtype=torch.float32)
     ra.device_error()
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    assert torch.equal(out32.view(torch.int32), out2_32.view(torch.int32))
 
 
 @pytest.mark.parametrize("name,layout", [("gqa4k", "zigzag"), ("s32k", "contiguous"),
@@ -106,17 +113,22 @@ def test_work_counters_match_host_scheduler_and_oracle(name, layout):
                                          ("s128k", "zigzag"), ("stress", "zigzag")])
 def test_large_workloads_sampled_rows(name, layout):
     w = WORKLOADS[name]
-    (q, k, v, offsets), (out, lse) = _run(w, layout)
+    (q, k, v, offsets), (out32, lse) = _run(w, layout, out_dtype=torch.float32)
+    out, lse_b = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, layout, w.causal, "fused",
+                                 scale=w.scale)
+    ra.device_error()
+    parity.check_rounding(out, out32, f"{name}/{layout}")
+    assert torch.equal(lse.view(torch.int32), lse_b.view(torch.int32))
     extra = []
     for rows in offsets.values():
         extra.extend(rows.tolist())
     rows = parity.sample_rows(w.S, w.c, layout, w.seed, extra=extra[:64])
     ref, ref_lse = _oracle_rows(q, k, v, w, rows)
-    got = _np(out[:, torch.as_tensor(rows)])
+    got = _np(out32[:, torch.as_tensor(rows)])
     parity.check_bf16(got, ref, f"{name}/{layout} out")
     parity.check_lse(_np(lse[:, :, torch.as_tensor(rows)]), ref_lse, f"{name}/{layout} lse")
     # properties that hold for every row: finite, and |out| bounded by max |v|
-    o = out.float()
+    o = out32
     assert torch.isfinite(o).all()
     assert o.abs().max().item() <= v.float().abs().max().item() * (1 + 1e-2) + 1e-2
     assert torch.isfinite(lse).all()

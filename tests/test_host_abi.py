@@ -63,7 +63,8 @@ def _shape(B=1, S=256, Hq=4, Hkv=2, D=128, dtype=ra.BF16, scale=0.088):
     (_shape(), 2, 5, -1),                         # unknown layout
 ])
 def test_ring_forward_rejects_bad_arguments_before_launch(lib, shape, c, layout, code):
-    st = lib.ra_ring_forward(None, None, None, shape, c, layout, 1, 0, None, None, None, 0, None, None)
+    st = lib.ra_ring_forward(None, None, None, shape, c, layout, 1, 0, shape.dtype, None, None, None,
+                             0, None, None)
     assert st == code
     assert lib.ra_ring_forward_workspace_size(shape, c, layout, 0) == 0
 
@@ -79,8 +80,11 @@ def test_null_pointers_and_workspace_are_rejected(lib):
     # aligned inputs but no workspace
     ok = ctypes.c_void_p(0x100000)
     assert lib.ra_ring_prepare(ok, ok, ok, shp, 2, ra.ZIGZAG, None, 0, None) == -5
-    assert lib.ra_ring_attend(shp, 2, ra.ZIGZAG, 1, 0, ok, None, ok, 10, 0, None) == -5
-    assert lib.ra_ring_attend(shp, 2, ra.ZIGZAG, 1, 9, ok, None, ok, 10, 0, None) == -1
+    assert lib.ra_ring_attend(shp, 2, ra.ZIGZAG, 1, 0, ra.BF16, ok, None, ok, 10, 0, None) == -5
+    assert lib.ra_ring_attend(shp, 2, ra.ZIGZAG, 1, 9, ra.BF16, ok, None, ok, 10, 0, None) == -1
+    # fp32 inputs cannot produce bf16 outputs
+    f32 = _shape(dtype=ra.F32)
+    assert lib.ra_ring_attend(f32, 2, ra.ZIGZAG, 1, 0, ra.BF16, ok, None, ok, 1 << 30, 0, None) == -1
     assert lib.ra_block_attn(None, None, None, None, None, 1, shp, None, None, None, None, None) == -1
     assert lib.ra_lse_merge(0, None, None, None, shp, None, None, None) == -1
     assert lib.ra_lse_merge(65, None, None, None, shp, None, None, None) == -1
@@ -89,8 +93,8 @@ def test_null_pointers_and_workspace_are_rejected(lib):
 def test_empty_problems_are_noops(lib):
     # B = 0 or S = 0: nothing to do, nothing launched, OK
     assert lib.ra_block_attn(None, None, None, None, None, 1, _shape(B=0), None, None, None, None, None) == 0
-    assert lib.ra_ring_forward(None, None, None, _shape(S=0), 2, ra.ZIGZAG, 1, 0, None, None, None, 0,
-                               None, None) == 0
+    assert lib.ra_ring_forward(None, None, None, _shape(S=0), 2, ra.ZIGZAG, 1, 0, ra.BF16, None, None,
+                               None, 0, None, None) == 0
     assert lib.ra_state_init(_shape(S=0), None, None, None, None) == 0
 
 
