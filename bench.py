@@ -55,6 +55,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, world, device=None):
+    """The largest of every rank's value (the job waits for the slowest rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(flop_per_rank_step, world, ms_per_step):
+    """Aggregate TFLOP/s of `world` ranks that each did one step of
+    `flop_per_rank_step` FLOP in `ms_per_step` (the max over ranks)."""
+    return world * flop_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -245,14 +262,10 @@ def run_ours(args, rank, world, local):
     ra.device_error()
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     attend_ms = [b.elapsed_time(c) for _, b, c in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     flop = w.flops()
-    value = world * flop / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_throughput(flop, world, ms_per_step)
 
     peaks, peak_kind = load_peaks()
     attn_ms = statistics.mean(attend_ms)
@@ -286,14 +299,10 @@ def run_ours(args, rank, world, local):
             b.record(stream)
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b))
-        e2e_ms = statistics.mean(times)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(statistics.mean(times), world, dev)
         bi = (q.numel() + k.numel() + v.numel()) * q.element_size()
         bo = oh.numel() * oh.element_size() + lh.numel() * 4
-        e2e = {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": whole_job_throughput(flop, world, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
 
     cpu = None

@@ -26,9 +26,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libra_gb300.so")
 
 BF16, F32 = 0, 1
-CONTIGUOUS, ZIGZAG = 0, 1
+CONTIGUOUS, ZIGZAG, STRIPED = 0, 1, 2
 MODE_FUSED, MODE_PER_STEP = 0, 1
-LAYOUTS = {"contiguous": CONTIGUOUS, "zigzag": ZIGZAG}
+LAYOUTS = {"contiguous": CONTIGUOUS, "zigzag": ZIGZAG, "striped": STRIPED}
 MODES = {"fused": MODE_FUSED, "per_step": MODE_PER_STEP}
 MERGE_MAX_PARTIALS = 64
 

@@ -529,46 +529,61 @@ __global__ void __maxnreg__(184)
           for (int i = 0; i < 128; ++i)
             if (!((bits[i >> 5] >> (i & 31)) & 1u)) sv[i] = 0xff800000u;
         }
-        // row maximum (four independent chains)
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        // row maximum: two chains of three-input max
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 128; i += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sv[i]));
-          mx1 = fmaxf(mx1, __uint_as_float(sv[i + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sv[i + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sv[i + 3]));
+          mx0 = ptx::fmax3(mx0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+          mx1 = ptx::fmax3(mx1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
         }
-        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        const float mx = fmaxf(mx0, mx1);
         const float m_new = fmaxf(m_run, mx * sl2);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
-        // probabilities, their sum, and P (bf16) over the first 64 columns of S
-        float sm0 = 0.f, sm1 = 0.f;
+        // probabilities in pairs: x = s*scale*log2e - m (paired fma), 2^x,
+        // the running sums of even and odd columns (paired add), and P (bf16)
+        // written over the first 64 columns of S
+        const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+        const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
+        uint64_t acc = ptx::f2_pack(0.f, 0.f);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float e0 = ptx::ex2(fmaf(__uint_as_float(sv[cc * 32 + 2 * i]), sl2, -m_use));
-            const float e1 = ptx::ex2(fmaf(__uint_as_float(sv[cc * 32 + 2 * i + 1]), sl2, -m_use));
-            sm0 += e0;
-            sm1 += e1;
+            const uint64_t x = ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[cc * 32 + 2 * i]),
+                                                        __uint_as_float(sv[cc * 32 + 2 * i + 1])),
+                                           sl2x2, negm2);
+            float x0, x1;
+            ptx::f2_unpack(x, x0, x1);
+            const float e0 = ptx::ex2(x0);
+            const float e1 = ptx::ex2(x1);
+            acc = ptx::f2_add(acc, ptx::f2_pack(e0, e1));
             pk[i] = ptx::pack_bf16x2(e0, e1);
           }
           ptx::tmem_st16(tS + cc * 16, pk);
         }
+        float sm0, sm1;
+        ptx::f2_unpack(acc, sm0, sm1);
         const float sum = sm0 + sm1;
         const float alpha = (m_run == m_new) ? 1.f : ptx::ex2(m_run - m_new);
         l_run = l_run * alpha + sum;
         // rescale the accumulator when the running maximum rose
         const bool need = (alpha != 1.f) && (m_run != -INFINITY);
         if (__any_sync(0xffffffffu, need)) {
+          const uint64_t a2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t u[32];
             ptx::tmem_ld32(tO + cc * 32, u);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              float y0, y1;
+              ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(u[i]), __uint_as_float(u[i + 1])), a2),
+                             y0, y1);
+              u[i] = __float_as_uint(y0);
+              u[i + 1] = __float_as_uint(y1);
+            }
             ptx::tmem_st32(tO + cc * 32, u);
           }
         }

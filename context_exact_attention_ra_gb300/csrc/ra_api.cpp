@@ -44,9 +44,9 @@ ra_status check_ring(const ra_shape& s, int c, int layout) {
   if (st != RA_OK) return st;
   if (s.Sq != s.Sk) return RA_ERR_INVALID;
   if (c < 1) return RA_ERR_INVALID;
-  if (layout != RA_CONTIGUOUS && layout != RA_ZIGZAG) return RA_ERR_INVALID;
+  if (layout != RA_CONTIGUOUS && layout != RA_ZIGZAG && layout != RA_STRIPED) return RA_ERR_INVALID;
   const long long S = s.Sq;
-  if (layout == RA_CONTIGUOUS && S % c != 0) return RA_ERR_INVALID;
+  if ((layout == RA_CONTIGUOUS || layout == RA_STRIPED) && S % c != 0) return RA_ERR_INVALID;
   if (layout == RA_ZIGZAG && S % (2LL * c) != 0) return RA_ERR_INVALID;
   return RA_OK;
 }

@@ -35,12 +35,13 @@ __global__ void zero_kernel(uint4* p, long long n16) {
 }
 
 // Natural row of local row `i` of rank `r` (contiguous: [r n, (r+1) n);
-// zig-zag: chunks r and 2c-1-r of length n/2).
+// zig-zag: chunks r and 2c-1-r of length n/2; striped: r + c i).
 __device__ __forceinline__ int natural_row(int r, int i, int n, int c, int layout) {
   if (layout == RA_ZIGZAG) {
     const int ch = n / 2;
     return i < ch ? r * ch + i : (2 * c - 1 - r) * ch + (i - ch);
   }
+  if (layout == RA_STRIPED) return r + c * i;
   return r * n + i;
 }
 

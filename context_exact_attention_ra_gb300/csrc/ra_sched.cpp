@@ -2,8 +2,9 @@
 // per-(rank, step) work, and the derived ring traffic and imbalance.
 //
 // Layouts: contiguous (rank k owns [kS/c, (k+1)S/c), "06 - Sequence / Context
-// Parallelism", section 1) and zig-zag (2c chunks, rank k owns chunks k and
-// 2c-1-k, plate "Splitting the Sequence").  Schedule: at step t rank i holds
+// Parallelism", section 1), zig-zag (2c chunks, rank k owns chunks k and
+// 2c-1-k, plate "Splitting the Sequence") and striped (rank k owns positions
+// k mod c, the tutorial's section 5).  Schedule: at step t rank i holds
 // the block of rank (i - t) mod c (tutorial section 4).  Work: the tutorial's
 // exercise B and the plate's "1.94 times the average" compare per-rank causal
 // work; here it is counted per 128x128 tile pair from each tile's smallest
@@ -28,6 +29,8 @@ void shard_positions(int S, int c, int layout, int32_t* pos) {
       if (layout == RA_ZIGZAG) {
         const int ch = n / 2;
         nat = i < ch ? r * ch + i : (2 * c - 1 - r) * ch + (i - ch);
+      } else if (layout == RA_STRIPED) {
+        nat = r + c * i;
       } else {
         nat = r * n + i;
       }

@@ -69,8 +69,10 @@ typedef enum { RA_BF16 = 0, RA_F32 = 1 } ra_dtype;
 /* Shard layouts.  Contiguous: rank k owns tokens [k*S/c, (k+1)*S/c)
  * (tutorial, section 1).  Zig-zag: the sequence is cut into 2c chunks and
  * rank k (counted from 0) owns chunks k and 2c-1-k, in increasing position
- * (plate "Splitting the Sequence"). */
-typedef enum { RA_CONTIGUOUS = 0, RA_ZIGZAG = 1 } ra_layout;
+ * (plate "Splitting the Sequence").  Striped: round robin, rank k owns the
+ * tokens whose position is k mod c, in increasing position (tutorial
+ * section 5, "striped / zigzag attention"). */
+typedef enum { RA_CONTIGUOUS = 0, RA_ZIGZAG = 1, RA_STRIPED = 2 } ra_layout;
 
 /* How ra_ring_forward executes the ring.
  * RA_MODE_FUSED: one launch; each (rank, query tile, head) block walks the
@@ -172,7 +174,8 @@ size_t ra_ring_forward_workspace_size(ra_shape shp, int c, int layout, int mode)
 /* Full ring attention over c virtual ranks on this GPU:
  * ra_ring_prepare followed by ra_ring_attend.
  *   q, k, v    device, natural token order, [B, S, Hq|Hkv, D] in shp.dtype
- *   c          ranks, 1 <= c; S % c == 0 (contiguous) or S % (2c) == 0 (zig-zag)
+ *   c          ranks, 1 <= c; S % c == 0 (contiguous, striped) or S % (2c) == 0
+ *              (zig-zag)
  *   out_dtype  element type of out: shp.dtype, or RA_F32 to receive the
  *              float32 result before its rounding to bf16 (the bf16 output is
  *              exactly that result rounded to nearest even)

@@ -9,6 +9,10 @@ Shard layouts (which global token positions a rank owns, in local order):
     2c chunks and device k gets chunks k and 2c-1-k (also its "Terms" list).
     Reading: k counts from 0 (counting from 1 would leave chunk 2c unowned);
     the two chunks are concatenated in increasing position.
+  * striped - the tutorial's section 5 ("striped / zigzag attention":
+    tokens assigned to GPUs in an interleaved pattern; section 12 cites
+    Striped Attention).  Reading: round robin, rank k owns every token whose
+    position is k mod c, in increasing position.
 
 Ring schedule (tutorial section 4): every rank sends its held K/V to rank
 i+1 and receives from i-1 after each step, so at step t rank i holds the
@@ -32,6 +36,7 @@ import numpy as np
 
 CONTIGUOUS = "contiguous"
 ZIGZAG = "zigzag"
+STRIPED = "striped"
 
 
 def shard_positions(S, c, layout):
@@ -48,6 +53,10 @@ def shard_positions(S, c, layout):
         return [np.concatenate([np.arange(r * ch, (r + 1) * ch),
                                 np.arange((2 * c - 1 - r) * ch, (2 * c - r) * ch)]).astype(np.int64)
                 for r in range(c)]
+    if layout == STRIPED:
+        if S % c:
+            raise ValueError("striped split needs S divisible by c")
+        return [np.arange(r, S, c, dtype=np.int64) for r in range(c)]
     raise ValueError(f"unknown layout {layout!r}")
 
 

@@ -24,7 +24,7 @@ F32_REL = 1e-5
 
 def chunk_bounds(S, c, layout):
     """(start, end) of every chunk of the layout in natural order."""
-    parts = c if layout == "contiguous" else 2 * c
+    parts = 2 * c if layout == "zigzag" else c
     size = S // parts
     return [(i * size, (i + 1) * size) for i in range(parts)]
 
@@ -41,7 +41,7 @@ def sample_rows(S, c, layout, seed, extra=(), uniform=64, boundaries_per_rank=2)
         rows.update((a, b - 1))
     step = len(chunks) // c
     for r in range(c):
-        a, b = chunks[r * step] if layout == "contiguous" else chunks[r]
+        a, b = chunks[r] if layout == "zigzag" else chunks[r * step]
         edges = list(range(a + 128, b, 128))
         if edges:
             for e in rng.choice(edges, size=min(boundaries_per_rank, len(edges)), replace=False):

@@ -83,7 +83,8 @@ def test_gqa4k_full_parity_and_modes_agree_bitwise():
 
 
 @pytest.mark.parametrize("name,layout", [("gqa4k", "zigzag"), ("s32k", "contiguous"),
-                                         ("s32k", "zigzag"), ("tiny", "contiguous")])
+                                         ("s32k", "zigzag"), ("s32k", "striped"),
+                                         ("tiny", "contiguous")])
 def test_work_counters_match_host_scheduler_and_oracle(name, layout):
     w = WORKLOADS[name]
     _, (_, _, info) = _run(w, layout, "fused", report=True)
@@ -110,7 +111,8 @@ def test_work_counters_match_host_scheduler_and_oracle(name, layout):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name,layout", [("s32k", "contiguous"), ("s32k", "zigzag"),
-                                         ("s128k", "zigzag"), ("stress", "zigzag")])
+                                         ("s32k", "striped"), ("s128k", "zigzag"),
+                                         ("stress", "zigzag")])
 def test_large_workloads_sampled_rows(name, layout):
     w = WORKLOADS[name]
     (q, k, v, offsets), (out32, lse) = _run(w, layout, out_dtype=torch.float32)
@@ -146,6 +148,9 @@ def test_large_workloads_sampled_rows(name, layout):
     (256, 64, "zigzag", True, 1, 2, 1, 128, "bf16"),        # chunks of 2 rows
     (384, 3, "zigzag", True, 1, 2, 1, 128, "f32"),          # fp32, D = 128, ragged tiles
     (200, 4, "contiguous", True, 2, 4, 2, 64, "f32"),
+    (1024, 4, "striped", True, 1, 4, 2, 128, "bf16"),       # round-robin tokens
+    (1000, 8, "striped", True, 2, 2, 1, 64, "bf16"),        # ragged striped shards
+    (384, 3, "striped", True, 1, 2, 1, 128, "f32"),
 ])
 def test_edge_cases_full_parity(S, c, layout, causal, B, Hq, Hkv, D, dtype):
     w = small_case(S, c, layout, causal, B=B, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, seed=S + c)

@@ -61,6 +61,7 @@ def _shape(B=1, S=256, Hq=4, Hkv=2, D=128, dtype=ra.BF16, scale=0.088):
     (_shape(scale=float("nan")), 2, ra.CONTIGUOUS, -1),
     (_shape(), 0, ra.CONTIGUOUS, -1),             # no ranks
     (_shape(), 2, 5, -1),                         # unknown layout
+    (_shape(S=250), 3, ra.STRIPED, -1),           # striped needs S divisible by c
 ])
 def test_ring_forward_rejects_bad_arguments_before_launch(lib, shape, c, layout, code):
     st = lib.ra_ring_forward(None, None, None, shape, c, layout, 1, 0, shape.dtype, None, None, None,
@@ -104,7 +105,8 @@ def test_schedule_matches_oracle(lib, c):
 
 
 @pytest.mark.parametrize("S,c,layout", [(256, 4, "contiguous"), (4096, 4, "zigzag"),
-                                        (1000, 5, "zigzag"), (96, 3, "contiguous")])
+                                        (1000, 5, "zigzag"), (96, 3, "contiguous"),
+                                        (96, 3, "striped"), (4096, 16, "striped")])
 def test_shard_positions_match_oracle(lib, S, c, layout):
     got = ra.shard_positions(S, c, layout)
     want = np.concatenate(ring.shard_positions(S, c, layout)).tolist()
@@ -114,7 +116,8 @@ def test_shard_positions_match_oracle(lib, S, c, layout):
 @pytest.mark.parametrize("S,c,layout,causal", [
     (256, 4, "contiguous", False), (4096, 4, "zigzag", True), (32768, 8, "contiguous", True),
     (32768, 8, "zigzag", True), (1000, 5, "zigzag", True), (600, 2, "contiguous", True),
-    (65536, 8, "zigzag", True)])
+    (65536, 8, "zigzag", True), (4096, 4, "striped", True), (1000, 8, "striped", True),
+    (32768, 8, "striped", True)])
 def test_expected_work_matches_oracle(lib, S, c, layout, causal):
     got = ra.work_expected(S, c, layout, causal)
     want = ring.work_table(S, c, layout, causal)

@@ -140,7 +140,7 @@ def test_scale_enters_as_a_temperature():
 # The exactness invariant: any ring order == full softmax
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
 @pytest.mark.parametrize("c", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("causal", [True, False])
 def test_ring_equals_full_softmax(layout, c, causal):
@@ -226,7 +226,7 @@ def test_merge_single_partial_is_plain_normalisation():
 @pytest.mark.parametrize("c", [1, 2, 4, 16])
 def test_layouts_partition_the_sequence(c):
     S = 64 * c
-    for layout in ("contiguous", "zigzag"):
+    for layout in ("contiguous", "zigzag", "striped"):
         shards = ring.shard_positions(S, c, layout)
         allpos = np.sort(np.concatenate(shards))
         assert np.array_equal(allpos, np.arange(S))
@@ -269,6 +269,18 @@ def test_contiguous_pair_counts_closed_form(S, c):
     # rank r sees r full blocks plus its own causal triangle
     assert per_rank == [r * n * n + n * (n + 1) // 2 for r in range(c)]
     assert abs(ring.imbalance(per_rank) - ((2 * c - 1) * n + 1) / (c * n + 1)) < 1e-15
+
+
+@pytest.mark.parametrize("S,c", [(64, 4), (4096, 4), (32768, 8), (131072, 16)])
+def test_striped_pair_counts_closed_form(S, c):
+    # rank k's a-th query sits at position k + c*a and sees k + c*a + 1 keys,
+    # so rank k sees c*n(n-1)/2 + n(k+1) pairs: nearly, not exactly, equal
+    n = S // c
+    shards = ring.shard_positions(S, c, "striped")
+    assert all(np.array_equal(shards[k], np.arange(k, S, c)) for k in range(c))
+    per_rank = [sum(ring.visible_pairs(shards[i], shards[j], True) for j in range(c)) for i in range(c)]
+    assert per_rank == [c * n * (n - 1) // 2 + n * (k + 1) for k in range(c)]
+    assert ring.imbalance(per_rank) < 1 + 1.0 / n
 
 
 @pytest.mark.parametrize("S,c", [(4096, 4), (32768, 8), (131072, 16), (65536, 8)])
