@@ -45,6 +45,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--overlap-study", action="store_true",
+                    help="time the ring with real K/V rotation, overlapped and not")
+    ap.add_argument("--decode", action="store_true",
+                    help="time decode over the sharded keys (one new token per step) instead")
     return ap.parse_args()
 
 
@@ -334,9 +338,119 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
 
 
+def run_decode(args, rank, world, local):
+    """Decode over distributed keys and values: one new token's 16 query heads
+    against the s128k keys and values held in 16 zig-zag shards (split-K
+    partials per shard piece + merge).  HBM-bound: the algorithmic bytes of a
+    step are one read of K and V plus q, out and lse."""
+    import torch
+
+    import context_exact_attention_ra_gb300 as ra
+    from workloads import WORKLOADS
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    layout = args.layout or w.layouts[0]
+    g = torch.Generator().manual_seed(w.seed)
+    k = torch.randn((w.B, w.S, w.Hkv, w.D), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((w.B, w.S, w.Hkv, w.D), generator=g).to(torch.bfloat16).to(dev)
+    q = torch.randn((w.B, 1, w.Hq, w.D), generator=g).to(torch.bfloat16).to(dev)
+    q_pos = torch.tensor([w.S - 1], dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ra.decode_forward(q, q_pos, k, v, w.c, layout, True)
+    ra.device_error()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ra.decode_forward(q, q_pos, k, v, w.c, layout, True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ra.device_error()
+    ms = statistics.median(times)
+    nbytes = 2 * k.numel() * k.element_size() + 2 * q.numel() * q.element_size() + w.B * w.Hq * 4
+    peaks, kind = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "decode over distributed KV: achieved GB/s (one token, K/V read once)",
+        "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode: 1 token, {w.name} keys S={w.S} c={w.c} {layout} Hq={w.Hq} "
+                               f"Hkv={w.Hkv} D={w.D}", "l2": "flushed before every step"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
+                     "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                     "kernel": "decode_partial_kernel + decode_merge_kernel"},
+        "gpu_launches": 2 * args.steps}), flush=True)
+
+
+def run_overlap_study(args, rank, world, local):
+    """The tutorial's exercise C on one GPU: the ring with its K/V pass made
+    real (device-to-device rotation between steps), with the copies on a
+    second stream overlapped with the attention, and serialised."""
+    import torch
+
+    import context_exact_attention_ra_gb300 as ra
+    from workloads import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    layout = args.layout or w.layouts[0]
+    q, k, v, _ = make_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    shp = ra.Shape(w.B, w.S, w.S, w.Hq, w.Hkv, w.D, ra.BF16 if w.dtype == "bf16" else ra.F32, w.scale)
+    ws = torch.empty(int(ra.lib().ra_ring_rotate_workspace_size(shp, w.c, ra.LAYOUTS[layout])),
+                     dtype=torch.uint8, device=dev)
+    copy_stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, fn in (("per_step", lambda: ra.ring_forward(qd, kd, vd, w.c, layout, w.causal, "per_step", scale=w.scale)),
+                     ("rotate_serial", lambda: ra.ring_forward_rotate(qd, kd, vd, w.c, layout, w.causal, False,
+                                                                      scale=w.scale, workspace=ws)),
+                     ("rotate_overlap", lambda: ra.ring_forward_rotate(qd, kd, vd, w.c, layout, w.causal, True,
+                                                                       scale=w.scale, workspace=ws,
+                                                                       copy_stream=copy_stream))):
+        for _ in range(args.warmup):
+            fn()
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.median(times)
+    ra.device_error()
+    kv_bytes_per_step = 2 * k.numel() * k.element_size()
+    print(json.dumps({
+        "metric": "ring step time with the K/V rotation overlapped vs serialised (ms per ring)",
+        "unit": "ms", "steps": args.steps, "warmup": args.warmup,
+        "config": {"workload": f"{w.name}: S={w.S} c={w.c} {layout} Hq={w.Hq} Hkv={w.Hkv} D={w.D}"},
+        "ms": res, "overlap_saving_ms": res["rotate_serial"] - res["rotate_overlap"],
+        "rotation_bytes_per_step": kv_bytes_per_step, "ring_steps": w.c,
+        "flop": w.flops()}), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.overlap_study:
+        run_overlap_study(args, rank, world, local)
+        return
+    if args.decode:
+        run_decode(args, rank, world, local)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

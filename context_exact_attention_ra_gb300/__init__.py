@@ -27,16 +27,22 @@ LIB_PATH = os.path.join(HERE, "libra_gb300.so")
 
 BF16, F32 = 0, 1
 CONTIGUOUS, ZIGZAG, STRIPED = 0, 1, 2
-MODE_FUSED, MODE_PER_STEP = 0, 1
+MODE_FUSED, MODE_PER_STEP, MODE_ALLGATHER = 0, 1, 2
 LAYOUTS = {"contiguous": CONTIGUOUS, "zigzag": ZIGZAG, "striped": STRIPED}
-MODES = {"fused": MODE_FUSED, "per_step": MODE_PER_STEP}
+MODES = {"fused": MODE_FUSED, "per_step": MODE_PER_STEP, "allgather": MODE_ALLGATHER}
 MERGE_MAX_PARTIALS = 64
 
 
 class RaError(RuntimeError):
     def __init__(self, status, what):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} ({status})")
+        detail = ""
+        try:
+            detail = lib().ra_last_error().decode()
+        except Exception:  # library not loadable
+            pass
+        msg = f"{what}: {status_string(status)} ({status})"
+        super().__init__(f"{msg} [{detail}]" if detail and status in (-3, -4) else msg)
 
 
 class Shape(ctypes.Structure):
@@ -62,6 +68,7 @@ _P = ctypes.c_void_p
 _SIGS = {
     "ra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ra_version": (ctypes.c_char_p, []),
+    "ra_last_error": (ctypes.c_char_p, []),
     "ra_state_init": (ctypes.c_int, [Shape, _P, _P, _P, _P]),
     "ra_block_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int, Shape, _P, _P, _P, _P, _P]),
     "ra_lse_merge": (ctypes.c_int, [ctypes.c_int, _P, _P, _P, Shape, _P, _P, _P]),
@@ -80,6 +87,13 @@ _SIGS = {
     "ra_ring_forward_hostio": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P,
                                               ctypes.c_size_t, _P]),
+    "ra_ring_rotate_workspace_size": (ctypes.c_size_t, [Shape, ctypes.c_int, ctypes.c_int]),
+    "ra_ring_forward_rotate": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, _P, _P, _P, ctypes.c_size_t,
+                                              _P, _P]),
+    "ra_decode_workspace_size": (ctypes.c_size_t, [Shape, ctypes.c_int, ctypes.c_int]),
+    "ra_decode_forward": (ctypes.c_int, [_P, _P, _P, _P, Shape, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, _P, _P, _P, ctypes.c_size_t, _P]),
     "ra_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int32)]),
     "ra_shard_positions": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_int32)]),
@@ -266,6 +280,53 @@ def ring_forward_hostio(q_host, k_host, v_host, c, layout="zigzag", causal=True,
 def hostio_workspace_size(shape: Shape, c, layout, mode, out_dtype_code=None):
     oc = shape.dtype if out_dtype_code is None else out_dtype_code
     return int(lib().ra_ring_forward_hostio_workspace_size(shape, int(c), int(layout), int(mode), oc))
+
+
+def ring_forward_rotate(q, k, v, c, layout="zigzag", causal=True, overlap=True, scale=None,
+                        out_dtype=None, workspace=None, stream=None, copy_stream=None):
+    """The ring with real K/V rotation between steps (device-to-device
+    copies), overlapped with the attention on ``copy_stream`` or not."""
+    _contig(q, k, v)
+    lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    shp = _shape(q, k, scale)
+    ocode, odt = _out_code(out_dtype, q)
+    out = torch.empty(q.shape, dtype=odt, device=q.device)
+    lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = int(lib().ra_ring_rotate_workspace_size(shp, int(c), lay))
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if overlap and copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=q.device)
+    cs = ctypes.c_void_p(copy_stream.cuda_stream) if (overlap and copy_stream is not None) else ctypes.c_void_p(0)
+    st = lib().ra_ring_forward_rotate(_ptr(q), _ptr(k), _ptr(v), shp, int(c), lay, int(bool(causal)),
+                                      int(bool(overlap)), ocode, _ptr(out), _ptr(lse), _ptr(workspace),
+                                      workspace.numel(), _stream(stream), cs)
+    _check(st, "ra_ring_forward_rotate")
+    return out, lse
+
+
+def decode_forward(q, q_pos, k, v, c, layout="zigzag", causal=True, scale=None, out_dtype=None,
+                   workspace=None, stream=None):
+    """Attention of a few new tokens' queries q [B,R,Hq,D] (positions q_pos,
+    int32 [R]) over k, v [B,S,Hkv,D] held in c shards: split-K partials per
+    shard piece, then their merge.  Returns (out [B,R,Hq,D], lse [B,Hq,R])."""
+    _contig(q, k, v)
+    lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    B, R, Hq, D = q.shape
+    shp = Shape(B, R, k.shape[1], Hq, k.shape[2], D, _dtype_code(q), float(scale))
+    ocode, odt = _out_code(out_dtype, q)
+    out = torch.empty((B, R, Hq, D), dtype=odt, device=q.device)
+    lse = torch.empty((B, Hq, R), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = int(lib().ra_decode_workspace_size(shp, int(c), lay))
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().ra_decode_forward(_ptr(q), _ptr(q_pos), _ptr(k), _ptr(v), shp, int(c), lay,
+                                 int(bool(causal)), ocode, _ptr(out), _ptr(lse), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(st, "ra_decode_forward")
+    return out, lse
 
 
 def state_init(B, S, Hq, D, device="cuda", dtype_code=BF16, stream=None):

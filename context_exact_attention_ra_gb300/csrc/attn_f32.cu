@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kThreadsF32)
   const int qvalid = max(0, min(kRows, p.n_q - row0));
   const int ktiles = (p.n_k + kTile - 1) / kTile;
   const long long R = static_cast<long long>(p.c) * p.n_q;
-  const long long RK = static_cast<long long>(p.c) * p.n_k;
+  // rows of the key/value tensors: c shards of n_k, or one gathered buffer
+  const long long RK = p.kv_all ? static_cast<long long>(p.n_k) : static_cast<long long>(p.c) * p.n_k;
 
   const bool row_ok = r < qvalid;
   const long long qrow = static_cast<long long>(rank) * p.n_q + row0 + r;
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kThreadsF32)
   const float sl2 = p.scale_log2;
 
   for (int t = p.t_begin; t < p.t_end; ++t) {
-    int src = (rank - t) % p.c;
+    int src = p.kv_all ? 0 : (rank - t) % p.c;
     if (src < 0) src += p.c;
     const int32_t* kpos_src = p.k_pos + static_cast<long long>(src) * p.n_k;
     unsigned long long pairs = 0, nfull = 0, npart = 0, nskip = 0;
@@ -114,7 +115,8 @@ __global__ void __launch_bounds__(kThreadsF32)
           const int kk = e / D, d = e % D;
           float kv = 0.f, vv = 0.f;
           if (kk < nk) {
-            const long long krow = static_cast<long long>(src) * p.n_k + kt * kTile + sub + kk;
+            const long long krow = static_cast<long long>(p.kv_by_holder ? rank : src) * p.n_k +
+                                   kt * kTile + sub + kk;
             const long long off = ((static_cast<long long>(b) * RK + krow) * p.Hkv + g) * D + d;
             kv = kf[off];
             vv = vf[off];

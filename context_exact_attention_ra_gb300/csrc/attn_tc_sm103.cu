@@ -197,8 +197,14 @@ __device__ __forceinline__ int ring_src(int rank, int t, int c) {
   return s < 0 ? s + c : s;
 }
 
+// Key/value shard read at step t: the ring's (rank - t) mod c, or, in the
+// all-gather form, the whole gathered buffer (source 0, c*n_k rows).
+__device__ __forceinline__ int step_src(const AttnParams& p, int rank, int t) {
+  return p.kv_all ? 0 : ring_src(rank, t, p.c);
+}
+
 template <int D>
-__global__ void __maxnreg__(184)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -264,12 +270,12 @@ __global__ void __maxnreg__(184)
     const int total = nsteps * ktiles;
     if (p.k_ranges != nullptr) {
       for (int i = threadIdx.x; i < total; i += kThreads) {
-        const int src = ring_src(rank, p.t_begin + i / ktiles, p.c);
+        const int src = step_src(p, rank, p.t_begin + i / ktiles);
         ranges[i] = p.k_ranges[static_cast<long long>(src) * ktiles + i % ktiles];
       }
     } else {
       for (int i = warp; i < total; i += kThreads / 32) {
-        const int src = ring_src(rank, p.t_begin + i / ktiles, p.c);
+        const int src = step_src(p, rank, p.t_begin + i / ktiles);
         const int kt = i % ktiles;
         int mn, mx;
         warp_minmax(p.k_pos + static_cast<long long>(src) * p.n_k + kt * kTile,
@@ -307,7 +313,7 @@ __global__ void __maxnreg__(184)
     uint32_t j = 0;
     bool ok = !*abort_flag;
     for (int t = p.t_begin; t < p.t_end && ok; ++t) {
-      const int src = ring_src(rank, t, p.c);
+      const int src = step_src(p, rank, t);
       const int2* rs = step_ranges(t);
       for (int kt = 0; kt < ktiles; ++kt) {
         const KTile k = k_tile(p, src, kt, qt, lane, rs);
@@ -320,7 +326,8 @@ __global__ void __maxnreg__(184)
             ptx::mbar_arrive_expect_tx(bar(full0 + s), L::kTileBytes);
             for (int x = 0; x < L::kBoxes; ++x)
               ptx::tma_load_4d(stage0 + s * L::kTileBytes + x * L::kBoxBytes, map,
-                               bar(full0 + s), x * L::kBox, g, src * p.n_k + kt * kTile, b);
+                               bar(full0 + s), x * L::kBox, g,
+                               (p.kv_by_holder ? rank : src) * p.n_k + kt * kTile, b);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -367,7 +374,7 @@ __global__ void __maxnreg__(184)
 
     uint32_t j = 0;
     for (int t = p.t_begin; t < p.t_end && ok; ++t) {
-      const int src = ring_src(rank, t, p.c);
+      const int src = step_src(p, rank, t);
       const int2* rs = step_ranges(t);
       unsigned long long nfull = 0, npart = 0, nskip = 0;
       for (int kt = 0; kt < ktiles; ++kt) {
@@ -490,7 +497,7 @@ __global__ void __maxnreg__(184)
     uint32_t j = 0;
     bool ok = true;
     for (int t = p.t_begin; t < p.t_end && ok; ++t) {
-      const int src = ring_src(rank, t, p.c);
+      const int src = step_src(p, rank, t);
       const int2* rs = step_ranges(t);
       const int32_t* kpos_src = p.k_pos + static_cast<long long>(src) * p.n_k;
       unsigned long long pairs = 0;
@@ -722,15 +729,18 @@ int launch_d(const AttnParams& p, const void* q, const void* k, const void* v,
   std::memset(&mq, 0, sizeof(mq));
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
+  launch_stage() = "cuTensorMapEncodeTiled";
   int e = make_map(&mq, q, p.B, q_rows_total, p.Hq, D);
   if (!e) e = make_map(&mk, k, p.B, k_rows_total, p.Hkv, D);
   if (!e) e = make_map(&mv, v, p.B, k_rows_total, p.Hkv, D);
   if (e) return e;
   const int smem = Smem<D>::kDynamic;
+  launch_stage() = "cudaFuncSetAttribute (tensor-core kernel)";
   cudaError_t ce = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (ce != cudaSuccess) return static_cast<int>(ce);
   dim3 grid(static_cast<unsigned>(p.B * p.Hq), static_cast<unsigned>(p.c * p.q_blocks_per_rank));
+  launch_stage() = "tensor-core kernel launch";
   attn_fwd_tc_kernel<D><<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
   return static_cast<int>(cudaGetLastError());
 }

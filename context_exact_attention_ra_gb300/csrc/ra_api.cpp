@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <vector>
 
@@ -26,7 +27,17 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 int elem_bytes(int dtype) { return dtype == RA_F32 ? 4 : 2; }
 
-ra_status cuda_status(int e) { return e == 0 ? RA_OK : RA_ERR_CUDA; }
+thread_local char g_last_error[320] = "";
+
+// Record a failed CUDA call (where, error name, code, text) for ra_last_error().
+ra_status cuda_fail(int e, const char* where) {
+  const cudaError_t ce = static_cast<cudaError_t>(e);
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d): %s", where, cudaGetErrorName(ce),
+                e, cudaGetErrorString(ce));
+  return RA_ERR_CUDA;
+}
+
+ra_status cuda_status(int e) { return e == 0 ? RA_OK : cuda_fail(e, ra::launch_stage()); }
 
 ra_status check_shape(const ra_shape& s) {
   if (s.B < 0 || s.Sq < 0 || s.Sk < 0 || s.Hq <= 0 || s.Hkv <= 0) return RA_ERR_INVALID;
@@ -49,6 +60,10 @@ ra_status check_ring(const ra_shape& s, int c, int layout) {
   if ((layout == RA_CONTIGUOUS || layout == RA_STRIPED) && S % c != 0) return RA_ERR_INVALID;
   if (layout == RA_ZIGZAG && S % (2LL * c) != 0) return RA_ERR_INVALID;
   return RA_OK;
+}
+
+bool mode_ok(int mode) {
+  return mode == RA_MODE_FUSED || mode == RA_MODE_PER_STEP || mode == RA_MODE_ALLGATHER;
 }
 
 // Output element type: the input dtype, or float32 (the fp32 result before
@@ -121,6 +136,7 @@ AttnParams base_params(const ra_shape& s, int c, int n_q, int n_k, int causal) {
 ra_status launch_attn(const AttnParams& p, const ra_shape& s, long long q_rows, long long k_rows,
                       void* stream) {
   if (static_cast<long long>(p.c) * p.q_blocks_per_rank > 65535) return RA_ERR_UNSUPPORTED;
+  ra::launch_stage() = "kernel launch";
   int e = (s.dtype == RA_BF16) ? ra::launch_attn_tc(p, p.q, p.k, p.v, q_rows, k_rows, stream)
                                : ra::launch_attn_f32(p, stream);
   return cuda_status(e);
@@ -144,6 +160,8 @@ const char* ra_status_string(int status) {
 
 const char* ra_version(void) { return "ra-gb300 0.1 sm_103a"; }
 
+const char* ra_last_error(void) { return g_last_error; }
+
 ra_status ra_state_init(ra_shape shp, float* o, float* m, float* l, ra_stream_t stream) {
   ra_status st = check_shape(shp);
   if (st != RA_OK) return st;
@@ -163,7 +181,7 @@ ra_status ra_block_attn(const void* q, const void* k, const void* v, const int32
   if ((reinterpret_cast<uintptr_t>(work) & 7u) != 0) return RA_ERR_INVALID;
   int err = 0;
   unsigned int* ew = ra::device_error_word(&err);
-  if (ew == nullptr) return RA_ERR_CUDA;
+  if (ew == nullptr) return cuda_fail(err, "device error word lookup");
   AttnParams p = base_params(shp, 1, shp.Sq, shp.Sk, causal);
   p.q_pos = q_pos;
   p.k_pos = k_pos;
@@ -207,7 +225,7 @@ ra_status ra_lse_merge(int P, const float* const* outs, const float* const* ms,
 
 size_t ra_ring_forward_workspace_size(ra_shape shp, int c, int layout, int mode) {
   if (check_ring(shp, c, layout) != RA_OK) return 0;
-  if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return 0;
+  if (!mode_ok(mode)) return 0;
   return ring_ws(shp, c, mode).total;
 }
 
@@ -224,17 +242,17 @@ ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape 
   int e = ra::launch_pack(q, k, v, shp.B, shp.Sq, shp.Hq, shp.Hkv, shp.D, elem_bytes(shp.dtype),
                           c, layout, at<void>(workspace, w.qp), at<void>(workspace, w.kp),
                           at<void>(workspace, w.vp), at<int32_t>(workspace, w.pos), stream);
-  if (e) return RA_ERR_CUDA;
+  if (e) return cuda_fail(e, ra::launch_stage());
   const int n = shp.Sq / c;
   e = ra::launch_tile_ranges(at<int32_t>(workspace, w.pos), c, n, at<int2>(workspace, w.ranges),
                              stream);
-  if (e) return RA_ERR_CUDA;
+  if (e) return cuda_fail(e, ra::launch_stage());
   // Heavy-first block order (used by causal calls): depends on positions only.
   const int total_blocks = c * blocks_per_rank(shp, n);
   if (total_blocks > 1 && total_blocks <= ra::kMaxOrderedBlocks) {
     e = ra::launch_block_order(at<int32_t>(workspace, w.pos), c, n, rows_per_block(shp.dtype),
                                blocks_per_rank(shp, n), at<int32_t>(workspace, w.order), stream);
-    if (e) return RA_ERR_CUDA;
+    if (e) return cuda_fail(e, ra::launch_stage());
   }
   return RA_OK;
 }
@@ -244,7 +262,7 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
                          ra_stream_t stream) {
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
-  if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (!mode_ok(mode)) return RA_ERR_INVALID;
   if (!out_dtype_ok(shp, out_dtype)) return RA_ERR_INVALID;
   if (shp.B == 0 || shp.Sq == 0) return RA_OK;
   if (out == nullptr || !aligned16(out)) return RA_ERR_INVALID;
@@ -254,7 +272,7 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
     return RA_ERR_WORKSPACE;
   int err = 0;
   unsigned int* ew = ra::device_error_word(&err);
-  if (ew == nullptr) return RA_ERR_CUDA;
+  if (ew == nullptr) return cuda_fail(err, "device error word lookup");
 
   const int S = shp.Sq;
   const int n = S / c;
@@ -273,7 +291,7 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
   if (count_work) {
     p.work = at<ra_work>(workspace, w.work);
     int e = ra::launch_zero(p.work, static_cast<size_t>(c) * c * sizeof(ra_work), stream);
-    if (e) return RA_ERR_CUDA;
+    if (e) return cuda_fail(e, ra::launch_stage());
   }
   const int total_blocks = c * p.q_blocks_per_rank;
   if (causal && total_blocks <= ra::kMaxOrderedBlocks && total_blocks > 1)
@@ -284,6 +302,19 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
     p.finalize = 1;
     return launch_attn(p, shp, S, S, stream);
   }
+  if (mode == RA_MODE_ALLGATHER) {
+    // one step over the gathered keys: the rank-major buffer holds all c
+    // shards in rank order, i.e. exactly what an all-gather delivers
+    p.kv_all = 1;
+    p.n_k = S;
+    p.t_begin = 0;
+    p.t_end = 1;
+    p.finalize = 1;
+    // per-rank key-tile ranges coincide with the gathered buffer's tiles only
+    // when shards are whole tiles; otherwise the kernel reduces them itself
+    if (n % ra::kTile != 0) p.k_ranges = nullptr;
+    return launch_attn(p, shp, S, S, stream);
+  }
   // Per-step: state in the workspace, one launch per ring step, then out / l.
   p.o_state = at<float>(workspace, w.o);
   p.m_state = at<float>(workspace, w.m);
@@ -292,7 +323,7 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
   p.store_state = 1;
   p.finalize = 0;
   int e = ra::launch_state_init(shp.B, S, shp.Hq, shp.D, p.o_state, p.m_state, p.l_state, stream);
-  if (e) return RA_ERR_CUDA;
+  if (e) return cuda_fail(e, ra::launch_stage());
   for (int t = 0; t < c; ++t) {
     p.t_begin = t;
     p.t_end = t + 1;
@@ -317,17 +348,19 @@ ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const voi
   const RingWs w = ring_ws(shp, c, mode);
   if (workspace == nullptr || ws_bytes < w.total) return RA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return RA_ERR_CUDA;
-  if (cudaMemcpy(host_per_rank_step, static_cast<const char*>(workspace) + w.work,
-                 static_cast<size_t>(c) * c * sizeof(ra_work), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return RA_ERR_CUDA;
+  cudaError_t ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamSynchronize");
+  ce = cudaMemcpy(host_per_rank_step, static_cast<const char*>(workspace) + w.work,
+                  static_cast<size_t>(c) * c * sizeof(ra_work), cudaMemcpyDeviceToHost);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemcpy (work counters)");
   return RA_OK;
 }
 
 ra_status ra_device_error(ra_stream_t stream) {
   unsigned int v = 0;
   int e = ra::read_and_clear_error(stream, &v);
-  if (e) return RA_ERR_CUDA;
+  if (e) return cuda_fail(e, "device error word read");
+  if (v) std::snprintf(g_last_error, sizeof(g_last_error), "device wait timed out (error bits 0x%x)", v);
   return v ? RA_ERR_TIMEOUT : RA_OK;
 }
 
@@ -362,7 +395,7 @@ ra_status ra_ring_forward(const void* q, const void* k, const void* v, ra_shape 
                           ra_stream_t stream) {
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
-  if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (!mode_ok(mode)) return RA_ERR_INVALID;
   if (!out_dtype_ok(shp, out_dtype)) return RA_ERR_INVALID;
   if (report != nullptr && report->c != c) return RA_ERR_INVALID;
   st = ra_ring_prepare(q, k, v, shp, c, layout, workspace, ws_bytes, stream);
@@ -414,6 +447,190 @@ ra_status ra_ring_forward(const void* q, const void* k, const void* v, ra_shape 
   return RA_OK;
 }
 
+namespace {
+// Partials of a decode call: P = c * pieces per shard.
+struct DecodeWs {
+  int P;
+  size_t o, m, l, total;
+};
+
+DecodeWs decode_ws(const ra_shape& s, int c) {
+  DecodeWs w;
+  const int n = s.Sk / c;
+  w.P = c * ra::decode_pieces_per_shard(n);
+  const size_t P = static_cast<size_t>(w.P), B = static_cast<size_t>(s.B), R = static_cast<size_t>(s.Sq);
+  size_t off = 0;
+  w.o = off;  off = round_up(off + P * B * R * s.Hq * s.D * sizeof(float));
+  w.m = off;  off = round_up(off + P * B * s.Hq * R * sizeof(float));
+  w.l = off;  off = round_up(off + P * B * s.Hq * R * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+ra_status check_decode(const ra_shape& s, int c, int layout) {
+  ra_status st = check_shape(s);
+  if (st != RA_OK) return st;
+  if (s.dtype != RA_BF16) return RA_ERR_UNSUPPORTED;
+  ra_shape ring = s;
+  ring.Sq = s.Sk;     // the key sequence must split over c like a ring's
+  return check_ring(ring, c, layout);
+}
+}  // namespace
+
+size_t ra_decode_workspace_size(ra_shape shp, int c, int layout) {
+  if (check_decode(shp, c, layout) != RA_OK || shp.Sk == 0) return 0;
+  return decode_ws(shp, c).total;
+}
+
+ra_status ra_decode_forward(const void* q, const int32_t* q_pos, const void* k, const void* v,
+                            ra_shape shp, int c, int layout, int causal, int out_dtype, void* out,
+                            float* lse, void* workspace, size_t ws_bytes, ra_stream_t stream) {
+  ra_status st = check_decode(shp, c, layout);
+  if (st != RA_OK) return st;
+  if (out_dtype != RA_BF16 && out_dtype != RA_F32) return RA_ERR_INVALID;
+  if (shp.B == 0 || shp.Sq == 0 || shp.Sk == 0) return RA_OK;
+  if (!q || !q_pos || !k || !v || !out) return RA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_INVALID;
+  const DecodeWs w = decode_ws(shp, c);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      ws_bytes < w.total)
+    return RA_ERR_WORKSPACE;
+  if (w.P > 65535) return RA_ERR_UNSUPPORTED;
+  ra::DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = shp.B;
+  p.R = shp.Sq;
+  p.S = shp.Sk;
+  p.n = shp.Sk / c;
+  p.c = c;
+  p.layout = layout;
+  p.Hq = shp.Hq;
+  p.Hkv = shp.Hkv;
+  p.D = shp.D;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(shp.scale) * kLog2e);
+  p.q = q;
+  p.q_pos = q_pos;
+  p.k = k;
+  p.v = v;
+  p.pieces_per_shard = ra::decode_pieces_per_shard(p.n);
+  p.P = w.P;
+  p.part_o = at<float>(workspace, w.o);
+  p.part_m = at<float>(workspace, w.m);
+  p.part_l = at<float>(workspace, w.l);
+  p.out = out;
+  p.out_f32 = out_dtype == RA_F32 ? 1 : 0;
+  p.lse = lse;
+  return cuda_status(ra::launch_decode(p, stream));
+}
+
+size_t ra_ring_rotate_workspace_size(ra_shape shp, int c, int layout) {
+  if (check_ring(shp, c, layout) != RA_OK) return 0;
+  const size_t base = ring_ws(shp, c, RA_MODE_PER_STEP).total;
+  const size_t kvb = static_cast<size_t>(shp.B) * shp.Sq * shp.Hkv * shp.D * elem_bytes(shp.dtype);
+  return base + 2 * round_up(kvb);
+}
+
+ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra_shape shp,
+                                 int c, int layout, int causal, int overlap, int out_dtype,
+                                 void* out, float* lse, void* workspace, size_t ws_bytes,
+                                 ra_stream_t stream, ra_stream_t copy_stream) {
+  ra_status st = check_ring(shp, c, layout);
+  if (st != RA_OK) return st;
+  if (!out_dtype_ok(shp, out_dtype)) return RA_ERR_INVALID;
+  if (overlap && (copy_stream == nullptr || copy_stream == stream)) return RA_ERR_INVALID;
+  if (shp.B == 0 || shp.Sq == 0) return RA_OK;
+  if (out == nullptr || !aligned16(out)) return RA_ERR_INVALID;
+  const size_t need = ra_ring_rotate_workspace_size(shp, c, layout);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      ws_bytes < need)
+    return RA_ERR_WORKSPACE;
+  int err = 0;
+  unsigned int* ew = ra::device_error_word(&err);
+  if (ew == nullptr) return cuda_fail(err, "device error word lookup");
+  st = ra_ring_prepare(q, k, v, shp, c, layout, workspace, ws_bytes, stream);
+  if (st != RA_OK) return st;
+
+  const RingWs w = ring_ws(shp, c, RA_MODE_PER_STEP);
+  const int S = shp.Sq, n = S / c;
+  const size_t slot_bytes = static_cast<size_t>(n) * shp.Hkv * shp.D * elem_bytes(shp.dtype);
+  const size_t batch_bytes = slot_bytes * c;
+  const size_t kvb = batch_bytes * shp.B;
+  char* kbuf[2] = {at<char>(workspace, w.kp), at<char>(workspace, w.total)};
+  char* vbuf[2] = {at<char>(workspace, w.vp), at<char>(workspace, w.total + round_up(kvb))};
+
+  AttnParams p = base_params(shp, c, n, n, causal);
+  p.q_pos = at<int32_t>(workspace, w.pos);
+  p.k_pos = p.q_pos;
+  p.k_ranges = at<int2>(workspace, w.ranges);
+  p.q = at<void>(workspace, w.qp);
+  p.err = ew;
+  p.kv_by_holder = 1;
+  p.o_state = at<float>(workspace, w.o);
+  p.m_state = at<float>(workspace, w.m);
+  p.l_state = at<float>(workspace, w.l);
+  p.load_state = 1;
+  p.store_state = 1;
+  if (causal && c * p.q_blocks_per_rank <= ra::kMaxOrderedBlocks && c * p.q_blocks_per_rank > 1)
+    p.block_order = at<int32_t>(workspace, w.order);
+  int e = ra::launch_state_init(shp.B, S, shp.Hq, shp.D, p.o_state, p.m_state, p.l_state, stream);
+  if (e) return cuda_fail(e, "state init launch");
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStream_t xs = overlap ? static_cast<cudaStream_t>(copy_stream) : cs;
+  cudaEvent_t ev_prep = nullptr, ev_copy = nullptr, ev_comp[2] = {nullptr, nullptr};
+  cudaError_t ce = cudaEventCreateWithFlags(&ev_prep, cudaEventDisableTiming);
+  if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&ev_copy, cudaEventDisableTiming);
+  if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&ev_comp[0], cudaEventDisableTiming);
+  if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&ev_comp[1], cudaEventDisableTiming);
+  if (ce == cudaSuccess && overlap) {
+    ce = cudaEventRecord(ev_prep, cs);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(xs, ev_prep, 0);
+  }
+  for (int t = 0; t < c && ce == cudaSuccess && st == RA_OK; ++t) {
+    if (t > 0 && overlap) ce = cudaStreamWaitEvent(cs, ev_copy, 0);   // block for step t arrived
+    if (ce != cudaSuccess) break;
+    p.k = kbuf[t & 1];
+    p.v = vbuf[t & 1];
+    p.t_begin = t;
+    p.t_end = t + 1;
+    st = launch_attn(p, shp, S, S, stream);
+    if (st != RA_OK) break;
+    ce = cudaEventRecord(ev_comp[t & 1], cs);
+    if (ce != cudaSuccess || t + 1 >= c) continue;
+    // SEND to i+1 / RECV from i-1: slot i of the next buffer gets slot i-1 of
+    // this one.  It overwrites what step t-1 read, so wait for that step.
+    if (overlap && t >= 1) ce = cudaStreamWaitEvent(xs, ev_comp[(t - 1) & 1], 0);
+    for (int b = 0; b < shp.B && ce == cudaSuccess; ++b) {
+      for (int which = 0; which < 2 && ce == cudaSuccess; ++which) {
+        char* src = (which ? vbuf : kbuf)[t & 1] + b * batch_bytes;
+        char* dst = (which ? vbuf : kbuf)[(t + 1) & 1] + b * batch_bytes;
+        if (c > 1) ce = cudaMemcpyAsync(dst + slot_bytes, src, slot_bytes * (c - 1),
+                                        cudaMemcpyDeviceToDevice, xs);
+        if (ce == cudaSuccess)
+          ce = cudaMemcpyAsync(dst, src + slot_bytes * (c - 1), slot_bytes,
+                               cudaMemcpyDeviceToDevice, xs);
+      }
+    }
+    if (ce == cudaSuccess && overlap) ce = cudaEventRecord(ev_copy, xs);
+  }
+  if (ev_prep) cudaEventDestroy(ev_prep);
+  if (ev_copy) cudaEventDestroy(ev_copy);
+  if (ev_comp[0]) cudaEventDestroy(ev_comp[0]);
+  if (ev_comp[1]) cudaEventDestroy(ev_comp[1]);
+  if (ce != cudaSuccess) return cuda_fail(ce, "ring rotation copies");
+  if (st != RA_OK) return st;
+  ra::MergeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.P = 1;
+  a.outs[0] = p.o_state;
+  a.ms[0] = p.m_state;
+  a.ls[0] = p.l_state;
+  ra::launch_stage() = "merge kernel launch";
+  return cuda_status(ra::launch_merge(a, shp.B, S, shp.Hq, shp.D, out_dtype, out, lse, p.q_pos, S,
+                                      stream));
+}
+
 size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode,
                                              int out_dtype) {
   const size_t base = ra_ring_forward_workspace_size(shp, c, layout, mode);
@@ -431,7 +648,7 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
                                  size_t ws_bytes, ra_stream_t stream) {
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
-  if (mode != RA_MODE_FUSED && mode != RA_MODE_PER_STEP) return RA_ERR_INVALID;
+  if (!mode_ok(mode)) return RA_ERR_INVALID;
   if (!out_dtype_ok(shp, out_dtype)) return RA_ERR_INVALID;
   if (shp.B == 0 || shp.Sq == 0) return RA_OK;
   if (!q_host || !k_host || !v_host || !out_host) return RA_ERR_INVALID;
@@ -452,17 +669,18 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
   void* dout = p; p += round_up(ob);
   float* dlse = reinterpret_cast<float*>(p);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return RA_ERR_CUDA;
+  cudaError_t ce = cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemcpyAsync (inputs)");
   st = ra_ring_forward(dq, dk, dv, shp, c, layout, causal, mode, out_dtype, dout,
                        lse_host ? dlse : nullptr, workspace, base, nullptr, stream);
   if (st != RA_OK) return st;
-  if (cudaMemcpyAsync(out_host, dout, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess) return RA_ERR_CUDA;
-  if (lse_host && cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return RA_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return RA_ERR_CUDA;
+  ce = cudaMemcpyAsync(out_host, dout, ob, cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess && lse_host) ce = cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemcpyAsync (outputs)");
+  ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamSynchronize");
   return RA_OK;
 }
 

@@ -25,6 +25,9 @@ struct AttnParams {
   int c;
   int n_q, n_k;                // rows per rank
   int t_begin, t_end;          // ring steps handled by this launch
+  int kv_all;                  // 1: one step over all c*n_k key rows (all-gather), no ring
+  int kv_by_holder;            // 1: the block held at a step sits in the holder's slot of k, v
+                               //    (rows rank*n_k ..), its positions are the source's
   int q_blocks_per_rank;       // ceil(n_q / rows per block)
   int causal;
   float scale_log2;            // scale * log2(e)
@@ -53,6 +56,23 @@ struct AttnParams {
   ra_work* work;               // [c*c] (rank*c + step) or nullptr
   unsigned int* err;           // device error word
   const int32_t* block_order;  // [c*q_blocks_per_rank] or nullptr
+};
+
+// Parameters of the decode (split-K over shards) kernels.
+struct DecodeParams {
+  int B, R, S, n, c, layout, Hq, Hkv, D, causal;
+  float scale_log2;
+  const void* q;               // [B, R, Hq, D] bf16, the new tokens' queries
+  const int32_t* q_pos;        // [R] their global positions
+  const void* k;               // [B, S, Hkv, D] bf16, natural order
+  const void* v;
+  int pieces_per_shard, P;     // P = c * pieces_per_shard partials
+  float* part_o;               // [P, B, R, Hq, D]
+  float* part_m;               // [P, B, Hq, R] (base-2 units)
+  float* part_l;
+  void* out;                   // [B, R, Hq, D]
+  int out_f32;
+  float* lse;                  // [B, Hq, R] or nullptr
 };
 
 // Error bits written into the device error word.
@@ -87,7 +107,11 @@ struct MergeArgs {
 int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype, void* out,
                  float* lse, const int32_t* out_row, int S_out, void* stream);
 int launch_zero(void* ptr, size_t bytes, void* stream);
+int launch_decode(const DecodeParams& p, void* stream);
+int decode_pieces_per_shard(int n);
 unsigned int* device_error_word(int* cuda_err);
+// Name of the host step that produced the last launcher error (thread-local).
+const char*& launch_stage();
 int read_and_clear_error(void* stream, unsigned int* value);
 
 // ---- host scheduler (ra_sched.cpp) ------------------------------------

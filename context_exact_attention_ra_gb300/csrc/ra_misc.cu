@@ -277,6 +277,11 @@ int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype,
   return static_cast<int>(cudaGetLastError());
 }
 
+const char*& launch_stage() {
+  thread_local const char* stage = "kernel launch";
+  return stage;
+}
+
 unsigned int* device_error_word(int* cuda_err) {
   // One address per device; looked up with that device current.
   static unsigned int* cache[64] = {nullptr};

@@ -81,8 +81,12 @@ typedef enum { RA_CONTIGUOUS = 0, RA_ZIGZAG = 1, RA_STRIPED = 2 } ra_layout;
  * RA_MODE_PER_STEP: one launch per ring step t over all ranks; the state
  *   lives in the workspace between steps; a final normalisation pass.
  * Both visit the same tiles in the same order with the same arithmetic and
- * give bitwise identical results. */
-typedef enum { RA_MODE_FUSED = 0, RA_MODE_PER_STEP = 1 } ra_mode;
+ * give bitwise identical results.
+ * RA_MODE_ALLGATHER: the all-gather form of context parallelism the plate
+ *   "Splitting the Sequence" reports for Llama 3: every rank gathers all c
+ *   shards and attends its queries to them in one step (no ring; work counts
+ *   are reported at step 0).  Same result up to rounding. */
+typedef enum { RA_MODE_FUSED = 0, RA_MODE_PER_STEP = 1, RA_MODE_ALLGATHER = 2 } ra_mode;
 
 typedef struct {
   int32_t B;       /* batch                                   */
@@ -127,6 +131,11 @@ const char* ra_status_string(int status);
 
 /* Library version string, e.g. "ra-gb300 0.1 sm_103a". */
 const char* ra_version(void);
+
+/* Text of the last CUDA failure or device timeout seen by a call on this
+ * host thread ("" if none): the failing step, the CUDA error name and its
+ * description.  Owned by the library; valid until the next call. */
+const char* ra_last_error(void);
 
 /* Initialise an online-softmax state for Sq rows: o = 0, m = -inf, l = 0
  * (tutorial section 4, "out_i, m_i, l_i = initialize()").  o: device
@@ -223,6 +232,39 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
                                  ra_shape shp, int c, int layout, int causal, int mode,
                                  int out_dtype, void* out_host, float* lse_host, void* workspace,
                                  size_t ws_bytes, ra_stream_t stream);
+
+/* The ring with its K/V pass made real (tutorial section 4: "SEND K,V to
+ * GPU (i+1) mod N, RECV K,V from GPU (i-1) mod N", and the point that the
+ * SEND can be overlapped with the compute of the current block; section 10
+ * exercise C measures it with and without overlap).  Each rank's held block
+ * lives in its own slot of a double buffer; after step t every holder's slot
+ * receives the block of holder i-1 (device-to-device copies), and step t+1
+ * attends to what arrived.  With overlap != 0 the copies run on copy_stream
+ * while step t computes (ordered by events); with overlap == 0 they run on
+ * `stream` between the steps.  The attention arithmetic is that of
+ * RA_MODE_PER_STEP, so the results are bitwise identical to it.
+ *   copy_stream  a stream other than `stream` (used only when overlap != 0) */
+size_t ra_ring_rotate_workspace_size(ra_shape shp, int c, int layout);
+ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra_shape shp,
+                                 int c, int layout, int causal, int overlap, int out_dtype,
+                                 void* out, float* lse, void* workspace, size_t ws_bytes,
+                                 ra_stream_t stream, ra_stream_t copy_stream);
+
+/* Decode over keys and values spread across c shards (tutorial section 7:
+ * decode has one query per step, and attention over the distributed keys needs
+ * a gather of partial results, like a FlashDecoding split-K): every shard's
+ * keys are split into pieces, a partial state (o, m, l) is computed for each
+ * piece, and the partials are merged into the normalised output.
+ *   shp        B, Sq = R new tokens, Sk = S keys, Hq, Hkv, D, dtype (bf16), scale
+ *   q          device [B, R, Hq, D] bf16;  q_pos device int32 [R] global positions
+ *   k, v       device [B, S, Hkv, D] bf16, natural order; the shards are those of
+ *              `layout` over c ranks (S divisible as for ra_ring_forward)
+ *   out        device [B, R, Hq, D] in out_dtype (bf16 or RA_F32); lse [B, Hq, R] or NULL
+ *   workspace  device, >= ra_decode_workspace_size() bytes (the partials) */
+size_t ra_decode_workspace_size(ra_shape shp, int c, int layout);
+ra_status ra_decode_forward(const void* q, const int32_t* q_pos, const void* k, const void* v,
+                            ra_shape shp, int c, int layout, int causal, int out_dtype, void* out,
+                            float* lse, void* workspace, size_t ws_bytes, ra_stream_t stream);
 
 /* ---- host-side scheduler (no GPU needed) ------------------------------ */
 

@@ -150,6 +150,57 @@ def ring_attention(q, k, v, c, layout, causal, scale, order=None):
     return out_full, lse_full
 
 
+def allgather_attention(q, k, v, c, layout, causal, scale):
+    """The all-gather form of context parallelism in float64.
+
+    The plate "Splitting the Sequence" notes that Llama 3 gathers every
+    rank's keys and values instead of passing them round a ring.  Each rank
+    first collects all c shards (in rank order), then attends its queries to
+    the gathered keys once, with the causal mask by global position.
+    Returns (out [B,S,Hq,D], lse [B,Hq,S]) in natural order.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, S, Hq, D = q.shape
+    shards = shard_positions(S, c, layout)
+    gathered = np.concatenate(shards)                # all-gather: every shard, rank order
+    out_full = np.zeros((B, S, Hq, D))
+    lse_full = np.full((B, Hq, S), -np.inf)
+    for i in range(c):
+        qp = shards[i]
+        o, m, l = block_partial(q[:, qp], k[:, gathered], v[:, gathered], qp, gathered, causal, scale)
+        pos = l > 0
+        ls = np.where(pos, l, 1.0)
+        out_full[:, qp] = np.where(np.transpose(pos, (0, 2, 1))[..., None],
+                                   o / np.transpose(ls, (0, 2, 1))[..., None], 0.0)
+        with np.errstate(divide="ignore"):
+            lse_full[:, :, qp] = np.where(pos, m + np.log(ls), -np.inf)
+    return out_full, lse_full
+
+
+def decode_split_kv(q_new, q_pos, k, v, c, layout, causal, scale):
+    """Attention of a few new queries over keys and values spread over c
+    shards, in float64: every shard computes its partial state for the
+    queries (split over the keys), and the partials are gathered and merged
+    (the tutorial's section 7: decode over distributed keys and values needs a
+    gather of partial results, like a split-K).  q_new: [B, R, Hq, D];
+    q_pos: [R] global positions.  Returns (out [B,R,Hq,D], lse [B,Hq,R]) and
+    the per-shard partials (o, m, l) that were merged."""
+    from .merge import finalize_state, merge_states
+
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    S = k.shape[1]
+    parts = []
+    for kp in shard_positions(S, c, layout):
+        parts.append(block_partial(np.asarray(q_new, dtype=np.float64), k[:, kp], v[:, kp],
+                                   np.asarray(q_pos), kp, causal, scale))
+    O, M, L = merge_states([p[0] for p in parts], [p[1] for p in parts], [p[2] for p in parts])
+    out, lse = finalize_state(O, M, L)
+    return out, lse, parts
+
+
 def visible_pairs(qp, kp, causal):
     """Number of (query, key) pairs with k_pos <= q_pos (all pairs if not causal)."""
     qp = np.asarray(qp, dtype=np.int64)

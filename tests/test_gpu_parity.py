@@ -266,3 +266,108 @@ def test_hostio_equals_device_path():
     ra.ring_forward_hostio(qh, kh, vh, w.c, "zigzag", True, "fused", out_host=out_h, lse_host=lse_h)
     assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
     assert torch.equal(lse_h.view(torch.int32), lse_d.cpu().view(torch.int32))
+
+
+# ---------------------------------------------------------------------------
+# The all-gather form (one step over the gathered keys) and striped shards
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,layout", [("gqa4k", "zigzag"), ("tiny", "contiguous"),
+                                         ("gqa4k", "striped")])
+def test_allgather_mode_full_parity_and_counters(name, layout):
+    w = WORKLOADS[name]
+    q, k, v, _ = make_inputs(w)
+    out, lse, info = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, layout, w.causal,
+                                     "allgather", scale=w.scale, report=True)
+    ra.device_error()
+    ref, ref_lse = _oracle_rows(q, k, v, w, np.arange(w.S))
+    if w.dtype == "bf16":
+        parity.check_bf16(_np(out), ref, "allgather out")
+        parity.check_lse(_np(lse), ref_lse, "allgather lse")
+    else:
+        parity.check_f32(_np(out), ref, "allgather out")
+    # counters: rank i against the gathered keys, all at step 0
+    shards = ring.shard_positions(w.S, w.c, layout)
+    gathered = np.concatenate(shards)
+    for i in range(w.c):
+        got = info["per_rank_step"][i][0]
+        f, p_, s_ = ring.tile_classes(shards[i], gathered, w.causal)
+        pairs = ring.visible_pairs(shards[i], gathered, w.causal)
+        scale = w.B * w.Hq
+        assert (got["pairs"], got["full"], got["partial"], got["skipped"]) == \
+            (pairs * scale, f * scale, p_ * scale, s_ * scale)
+        assert all(info["per_rank_step"][i][t]["pairs"] == 0 for t in range(1, w.c))
+
+
+def test_allgather_large_sampled_rows():
+    w = WORKLOADS["s32k"]
+    q, k, v, _ = make_inputs(w)
+    out, lse = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, "allgather",
+                               scale=w.scale, out_dtype=torch.float32)
+    ra.device_error()
+    rows = parity.sample_rows(w.S, w.c, "zigzag", w.seed)
+    ref, ref_lse = _oracle_rows(q, k, v, w, rows)
+    parity.check_bf16(_np(out[:, torch.as_tensor(rows)]), ref, "allgather s32k out")
+    parity.check_lse(_np(lse[:, :, torch.as_tensor(rows)]), ref_lse, "allgather s32k lse")
+
+
+# ---------------------------------------------------------------------------
+# Decode over distributed keys: split-K partials per shard piece + merge
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S,c,layout,R,Hq,Hkv,D,B", [
+    (4096, 4, "zigzag", 1, 8, 2, 128, 1),        # one new token, GQA 4:1
+    (4096, 4, "contiguous", 4, 8, 2, 128, 2),    # a few tokens at mixed positions, batch 2
+    (3000, 5, "striped", 3, 6, 3, 64, 1),        # ragged pieces, D = 64
+    (131072, 16, "zigzag", 1, 16, 1, 128, 1),    # the s128k shape: 16 query heads share one KV head
+])
+def test_decode_split_kv_full_parity(S, c, layout, R, Hq, Hkv, D, B):
+    g = torch.Generator().manual_seed(S + R)
+    k = torch.randn((B, S, Hkv, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, S, Hkv, D), generator=g).to(torch.bfloat16)
+    q = torch.randn((B, R, Hq, D), generator=g).to(torch.bfloat16)
+    q_pos = np.array(sorted({S - 1, S // 2, 17, S // 3}))[:R] if R > 1 else np.array([S - 1])
+    q_pos = q_pos[:R]
+    out, lse = ra.decode_forward(q.to(DEV), torch.as_tensor(q_pos, dtype=torch.int32, device=DEV),
+                                 k.to(DEV), v.to(DEV), c, layout, True, out_dtype=torch.float32)
+    outb, _ = ra.decode_forward(q.to(DEV), torch.as_tensor(q_pos, dtype=torch.int32, device=DEV),
+                                k.to(DEV), v.to(DEV), c, layout, True)
+    ra.device_error()
+    scale = D ** -0.5
+    ref, ref_lse, _ = ring.decode_split_kv(_np(q), q_pos, _np(k), _np(v), c, layout, True, scale)
+    ref2, ref2_lse, _, _ = oracle.attention_reference(_np(q), _np(k), _np(v), q_pos, np.arange(S), True, scale)
+    assert np.allclose(ref, ref2, atol=1e-10)
+    # fp32 arithmetic throughout: the result is close to the float64 oracle
+    parity.check_bf16(_np(out), ref, "decode out")
+    assert np.abs(_np(out) - ref).max() <= 1e-4
+    parity.check_lse(_np(lse), ref_lse, "decode lse")
+    parity.check_rounding(outb, out, "decode")
+
+
+# ---------------------------------------------------------------------------
+# The ring with its K/V pass made real (device-to-device rotation), with and
+# without overlap: bitwise equal to the per-step mode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,layout,overlap", [("gqa4k", "zigzag", True), ("gqa4k", "zigzag", False),
+                                                 ("tiny", "contiguous", True), ("gqa4k", "striped", True)])
+def test_rotating_ring_equals_per_step(name, layout, overlap):
+    w = WORKLOADS[name]
+    q, k, v, _ = make_inputs(w)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    want, want_lse = ra.ring_forward(qd, kd, vd, w.c, layout, w.causal, "per_step", scale=w.scale)
+    got, got_lse = ra.ring_forward_rotate(qd, kd, vd, w.c, layout, w.causal, overlap, scale=w.scale)
+    torch.cuda.synchronize()
+    ra.device_error()
+    assert torch.equal(got.view(torch.uint8), want.view(torch.uint8))
+    assert torch.equal(got_lse.view(torch.int32), want_lse.view(torch.int32))
+
+
+def test_rotating_ring_ragged_batch():
+    w = small_case(1000, 5, "zigzag", True, B=2, Hq=4, Hkv=2, D=128, seed=41)
+    q, k, v, _ = make_inputs(w)
+    got, _ = ra.ring_forward_rotate(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, True)
+    torch.cuda.synchronize()
+    ra.device_error()
+    ref, _ = _oracle_rows(q, k, v, w, np.arange(w.S))
+    parity.check_bf16(_np(got), ref, "rotating ring out")

@@ -359,3 +359,33 @@ def test_plate_transfer_to_compute_ratio():
     flop = 4 * pairs * D * e["q_heads_per_device"]
     t_att = flop / (e["attention_efficiency"] * e["external_assumption_h100_dense_bf16_tflops"] * 1e12)
     assert round(t_net / t_att, e["decimals"]) == e["value"]
+
+
+# --------------------------------------------------------------------------
+# All-gather form and decode over distributed keys (next rows)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
+def test_allgather_equals_full_softmax(layout):
+    rng = np.random.default_rng(21)
+    S, c = 48, 4
+    q, k, v = _rand(rng, 2, S, 4, 5) * 3, _rand(rng, 2, S, 2, 5) * 3, _rand(rng, 2, S, 2, 5)
+    pos = np.arange(S)
+    ref, lse_ref, _, _ = oracle.attention_reference(q, k, v, pos, pos, True, 0.6)
+    out, lse = ring.allgather_attention(q, k, v, c, layout, True, 0.6)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
+def test_decode_split_kv_equals_full_softmax(layout):
+    rng = np.random.default_rng(22)
+    S, c, R = 64, 4, 3
+    k, v = _rand(rng, 1, S, 2, 6) * 2, _rand(rng, 1, S, 2, 6)
+    q_new = _rand(rng, 1, R, 8, 6) * 2
+    q_pos = np.array([S - 1, 40, 5])              # the newest token and two earlier ones
+    ref, lse_ref, _, _ = oracle.attention_reference(q_new, k, v, q_pos, np.arange(S), True, 0.4)
+    out, lse, parts = ring.decode_split_kv(q_new, q_pos, k, v, c, layout, True, 0.4)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-12)
+    assert len(parts) == c
