@@ -100,6 +100,8 @@ _SIGS = {
     "ra_work_expected": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(Work)]),
     "ra_device_error": (ctypes.c_int, [_P]),
+    "ra_ring_forward_noalloc": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
 }
 
 _lib = None
@@ -392,6 +394,30 @@ def work_expected(S, c, layout, causal):
     _check(lib().ra_work_expected(int(S), int(c), lay, int(bool(causal)), w), "ra_work_expected")
     return [[(w[i * c + t].pairs, w[i * c + t].tiles_full, w[i * c + t].tiles_partial,
               w[i * c + t].tiles_skipped) for t in range(c)] for i in range(c)]
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def ring_forward_noalloc(q, k, v, c, layout="zigzag", causal=True, mode="fused", scale=None,
+                         out=None, lse=None, stream=None):
+    """ring_forward through ra_ring_forward_noalloc: for callers that cannot
+    allocate device memory when attention runs, the library uses its own fixed
+    64 MiB scratch array instead of a workspace.  ``out`` and ``lse`` may be
+    passed in (then nothing at all is allocated by this call)."""
+    _contig(q, k, v)
+    lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    md = MODES[mode] if isinstance(mode, str) else int(mode)
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
+    st = lib().ra_ring_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _shape(q, k, scale), int(c), lay,
+                                       int(bool(causal)), md, _dtype_code(out), _ptr(out), _ptr(lse),
+                                       _stream(stream))
+    _check(st, "ra_ring_forward_noalloc")
+    return out, lse
 
 
 def device_error(stream=None):

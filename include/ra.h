@@ -233,6 +233,27 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
                                  int out_dtype, void* out_host, float* lse_host, void* workspace,
                                  size_t ws_bytes, ra_stream_t stream);
 
+/* ra_ring_forward for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this is a deployment convenience of this
+ * library.  Some callers cannot call cudaMalloc where they run attention
+ * (cudaMalloc may synchronise the device and may fail part-way through a
+ * job; some host frameworks own all device memory).  This entry point takes
+ * no workspace: its scratch is a fixed array of RA_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) that the library reserves on every GPU where it is used, until the
+ * process exits.  It allocates nothing itself (no cudaMalloc, cudaFree or
+ * allocating library call).
+ *   Arguments and results as ra_ring_forward (no report).
+ *   Problems whose workspace (ra_ring_forward_workspace_size) exceeds the
+ *   scratch are rejected with RA_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks up the scratch's device address; make
+ *   that first call before any stream capture.
+ *   All calls share the one scratch array: calls that overlap on the GPU
+ *   (other streams, other host threads on the same device) race. */
+#define RA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+ra_status ra_ring_forward_noalloc(const void* q, const void* k, const void* v, ra_shape shp,
+                                  int c, int layout, int causal, int mode, int out_dtype,
+                                  void* out, float* lse, ra_stream_t stream);
+
 /* The ring with its K/V pass made real (tutorial section 4: "SEND K,V to
  * GPU (i+1) mod N, RECV K,V from GPU (i-1) mod N", and the point that the
  * SEND can be overlapped with the compute of the current block; section 10
