@@ -536,64 +536,88 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 128; ++i)
             if (!((bits[i >> 5] >> (i & 31)) & 1u)) sv[i] = 0xff800000u;
         }
-        // row maximum: two chains of three-input max
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        // row maximum: eight independent chains of three-input max
+        float mc[8];
 #pragma unroll
-        for (int i = 0; i < 128; i += 4) {
-          mx0 = ptx::fmax3(mx0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
-          mx1 = ptx::fmax3(mx1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
+        for (int c = 0; c < 8; ++c)
+          mc[c] = ptx::fmax3(__uint_as_float(sv[16 * c]), __uint_as_float(sv[16 * c + 1]),
+                             __uint_as_float(sv[16 * c + 2]));
+#pragma unroll
+        for (int i = 3; i < 15; i += 2) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            mc[c] = ptx::fmax3(mc[c], __uint_as_float(sv[16 * c + i]), __uint_as_float(sv[16 * c + i + 1]));
         }
-        const float mx = fmaxf(mx0, mx1);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mc[c] = fmaxf(mc[c], __uint_as_float(sv[16 * c + 15]));
+        const float mx = ptx::fmax3(ptx::fmax3(mc[0], mc[1], mc[2]), ptx::fmax3(mc[3], mc[4], mc[5]),
+                                    fmaxf(mc[6], mc[7]));
         const float m_new = fmaxf(m_run, mx * sl2);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
-        // probabilities in pairs: x = s*scale*log2e - m (paired fma), 2^x,
-        // the running sums of even and odd columns (paired add), and P (bf16)
-        // written over the first 64 columns of S
-        const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
-        const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
-        uint64_t acc = ptx::f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint64_t x = ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[cc * 32 + 2 * i]),
-                                                        __uint_as_float(sv[cc * 32 + 2 * i + 1])),
-                                           sl2x2, negm2);
-            float x0, x1;
-            ptx::f2_unpack(x, x0, x1);
-            const float e0 = ptx::ex2(x0);
-            const float e1 = ptx::ex2(x1);
-            acc = ptx::f2_add(acc, ptx::f2_pack(e0, e1));
-            pk[i] = ptx::pack_bf16x2(e0, e1);
-          }
-          ptx::tmem_st16(tS + cc * 16, pk);
-        }
-        float sm0, sm1;
-        ptx::f2_unpack(acc, sm0, sm1);
-        const float sum = sm0 + sm1;
+        // rescale the accumulator when the running maximum rose; the previous
+        // P.V has completed (this tile's S was committed after it), and the
+        // next one is issued only after this tile's P is handed over
         const float alpha = (m_run == m_new) ? 1.f : ptx::ex2(m_run - m_new);
-        l_run = l_run * alpha + sum;
-        // rescale the accumulator when the running maximum rose
-        const bool need = (alpha != 1.f) && (m_run != -INFINITY);
-        if (__any_sync(0xffffffffu, need)) {
+        if (__any_sync(0xffffffffu, (alpha != 1.f) && (m_run != -INFINITY))) {
           const uint64_t a2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t u[32];
-            ptx::tmem_ld32(tO + cc * 32, u);
+          for (int half = 0; half < D / 64; ++half) {
+            uint32_t u[64];
+            ptx::tmem_ld64(tO + half * 64, u);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
+            for (int i = 0; i < 64; i += 2) {
               float y0, y1;
               ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(u[i]), __uint_as_float(u[i + 1])), a2),
                              y0, y1);
               u[i] = __float_as_uint(y0);
               u[i + 1] = __float_as_uint(y1);
             }
-            ptx::tmem_st32(tO + cc * 32, u);
+            uint32_t w0[32], w1[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              w0[i] = u[i];
+              w1[i] = u[32 + i];
+            }
+            ptx::tmem_st32(tO + half * 64, w0);
+            ptx::tmem_st32(tO + half * 64 + 32, w1);
           }
         }
+
+        const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+        const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
+        uint64_t acc = ptx::f2_pack(0.f, 0.f);
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sh[64];
+          ptx::tmem_ld64(tS + half * 64, sh);
+          if (masked) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (!((bits[half * 2 + (i >> 5)] >> (i & 31)) & 1u)) sh[i] = 0xff800000u;
+          }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint64_t x = ptx::f2_fma(ptx::f2_pack(__uint_as_float(sh[cc * 32 + 2 * i]),
+                                                          __uint_as_float(sh[cc * 32 + 2 * i + 1])),
+                                             sl2x2, negm2);
+              float x0, x1;
+              ptx::f2_unpack(x, x0, x1);
+              const float e0 = ptx::ex2(x0);
+              const float e1 = ptx::ex2(x1);
+              acc = ptx::f2_add(acc, ptx::f2_pack(e0, e1));
+              pk[i] = ptx::pack_bf16x2(e0, e1);
+            }
+            ptx::tmem_st16(tS + half * 32 + cc * 16, pk);
+          }
+        }
+        float sm0, sm1;
+        ptx::f2_unpack(acc, sm0, sm1);
+        const float sum = sm0 + sm1;
+        l_run = l_run * alpha + sum;
         m_run = m_new;
         if (row_ok) pairs += nvis;
         ptx::tmem_wait_st();

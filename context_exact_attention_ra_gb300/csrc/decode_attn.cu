@@ -7,7 +7,9 @@
 // block computes the partial online-softmax state (o, m, l) of all query rows
 // of one (batch, key/value head) -- the G query heads that share the head
 // times the R new tokens -- over one piece, so each key and value byte is read
-// from memory once.  A second kernel merges the partials of every query row.
+// from memory once.  A second kernel merges the partials of every query row
+// (one block per row).  Both combine partial sums in a fixed order, so the
+// results do not depend on timing.
 // The work per key is 2*G*R*D multiply-adds for R*G <= 16 rows, so the path
 // is bound by memory bandwidth (reading K and V once), not by arithmetic; it
 // runs on the CUDA cores in fp32.
@@ -180,28 +182,36 @@ __global__ void __launch_bounds__(kDecThreads)
   }
 
   // ---- combine the 8 warps' states into the block's partial: common max,
-  // then every warp adds its rescaled sums into shared memory
+  // then the warps add their rescaled sums into shared memory one after the
+  // other (a fixed order, so the result does not depend on timing)
   if (lane == 0) {
 #pragma unroll
     for (int r = 0; r < kDecRows; ++r) wm[warp][r] = m_run[r];
   }
   __syncthreads();
+  float fr[kDecRows], lr[kDecRows];
 #pragma unroll
   for (int r = 0; r < kDecRows; ++r) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w][r]);
-    const float f = (m_run[r] == -INFINITY) ? 0.f : exp2f(m_run[r] - M);
+    fr[r] = (m_run[r] == -INFINITY) ? 0.f : exp2f(m_run[r] - M);
     float l = l_lane[r];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    if (lane == 0 && f != 0.f) atomicAdd(&Ls[r], l * f);
-    if (f != 0.f) {
-#pragma unroll
-      for (int c = 0; c < VC; ++c) atomicAdd(&Os[r][lane * VC + c], acc[r][c] * f);
-    }
+    lr[r] = l;
   }
-  __syncthreads();
+  for (int w = 0; w < kDecWarps; ++w) {
+    if (warp == w) {
+#pragma unroll
+      for (int r = 0; r < kDecRows; ++r) {
+        if (lane == 0) Ls[r] += lr[r] * fr[r];
+#pragma unroll
+        for (int c = 0; c < VC; ++c) Os[r][lane * VC + c] += acc[r][c] * fr[r];
+      }
+    }
+    __syncthreads();
+  }
   for (int e = threadIdx.x; e < nrows * D; e += kDecThreads) {
     const int r = e / D, d = e % D;
     float M = -INFINITY;
@@ -221,45 +231,65 @@ __global__ void __launch_bounds__(kDecThreads)
   }
 }
 
-// One warp per (b, h, token): merge the P partials, normalise, write out and lse.
+// One block of 8 warps per (b, h, token): merge the P partials, normalise,
+// write out and lse.  The warps take every 8th partial; their sums are added
+// in warp order.
 template <int D>
-__global__ void decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads) decode_merge_kernel(const DecodeParams p) {
   constexpr int VC = D / 32;
-  const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  __shared__ float red[kDecWarps];
+  __shared__ float red_l[kDecWarps];
+  __shared__ float red_o[kDecWarps][D];
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const long long total = static_cast<long long>(p.B) * p.Hq * p.R;
-  if (wid >= total) return;
-  const int tok = static_cast<int>(wid % p.R);
-  const int h = static_cast<int>((wid / p.R) % p.Hq);
-  const int b = static_cast<int>(wid / (static_cast<long long>(p.R) * p.Hq));
+  const long long row = blockIdx.x;
+  const int tok = static_cast<int>(row % p.R);
+  const int h = static_cast<int>((row / p.R) % p.Hq);
+  const int b = static_cast<int>(row / (static_cast<long long>(p.R) * p.Hq));
+  auto mi = [&](int i) { return ((static_cast<long long>(i) * p.B + b) * p.Hq + h) * p.R + tok; };
   float M = -INFINITY;
-  for (int i = 0; i < p.P; ++i)
-    M = fmaxf(M, p.part_m[((static_cast<long long>(i) * p.B + b) * p.Hq + h) * p.R + tok]);
+  for (int i = threadIdx.x; i < p.P; i += kDecThreads) M = fmaxf(M, p.part_m[mi(i)]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < kDecWarps; ++w) M = fmaxf(M, red[w]);
   const float Mu = (M == -INFINITY) ? 0.f : M;
   float L = 0.f, acc[VC];
 #pragma unroll
   for (int c = 0; c < VC; ++c) acc[c] = 0.f;
-  for (int i = 0; i < p.P; ++i) {
-    const long long pm = ((static_cast<long long>(i) * p.B + b) * p.Hq + h) * p.R + tok;
-    const float mi = p.part_m[pm];
-    const float f = (mi == -INFINITY) ? 0.f : exp2f(mi - Mu);
-    L = fmaf(p.part_l[pm], f, L);
+#pragma unroll 4
+  for (int i = warp; i < p.P; i += kDecWarps) {
+    const float m = p.part_m[mi(i)];
+    const float f = (m == -INFINITY) ? 0.f : exp2f(m - Mu);
+    L = fmaf(p.part_l[mi(i)], f, L);
     const float* po = p.part_o + (((static_cast<long long>(i) * p.B + b) * p.R + tok) * p.Hq + h) * D + lane * VC;
 #pragma unroll
     for (int c = 0; c < VC; ++c) acc[c] = fmaf(po[c], f, acc[c]);
   }
-  const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  const long long od = ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * D + lane * VC;
-  if (p.out_f32) {
+  if (lane == 0) red_l[warp] = L;
 #pragma unroll
-    for (int c = 0; c < VC; ++c) static_cast<float*>(p.out)[od + c] = acc[c] * inv;
-  } else {
+  for (int c = 0; c < VC; ++c) red_o[warp][lane * VC + c] = acc[c];
+  __syncthreads();
+  float Lt = 0.f;
 #pragma unroll
-    for (int c = 0; c < VC; ++c) static_cast<__nv_bfloat16*>(p.out)[od + c] = __float2bfloat16_rn(acc[c] * inv);
+  for (int w = 0; w < kDecWarps; ++w) Lt += red_l[w];
+  const float inv = (Lt > 0.f) ? 1.f / Lt : 0.f;
+  const long long od = ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * D;
+  for (int d = threadIdx.x; d < D; d += kDecThreads) {
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) o += red_o[w][d];
+    if (p.out_f32)
+      static_cast<float*>(p.out)[od + d] = o * inv;
+    else
+      static_cast<__nv_bfloat16*>(p.out)[od + d] = __float2bfloat16_rn(o * inv);
   }
-  if (lane == 0 && p.lse != nullptr)
+  if (threadIdx.x == 0 && p.lse != nullptr)
     p.lse[(static_cast<long long>(b) * p.Hq + h) * p.R + tok] =
-        (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        (Lt > 0.f) ? (M + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace
@@ -279,13 +309,12 @@ int launch_decode(const DecodeParams& p, void* stream) {
     decode_partial_kernel<64><<<grid, kDecThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
-  const long long warps = static_cast<long long>(p.B) * p.Hq * p.R;
-  const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
+  const unsigned rows = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hq * p.R);
   launch_stage() = "decode merge kernel launch";
   if (p.D == 128)
-    decode_merge_kernel<128><<<blocks, 256, 0, s>>>(p);
+    decode_merge_kernel<128><<<rows, kDecThreads, 0, s>>>(p);
   else
-    decode_merge_kernel<64><<<blocks, 256, 0, s>>>(p);
+    decode_merge_kernel<64><<<rows, kDecThreads, 0, s>>>(p);
   return static_cast<int>(cudaGetLastError());
 }
 
