@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kDecRows = 16;     // query rows (G heads x R tokens) per block
+constexpr int kDecRows = 8;      // query rows (G heads x R tokens) per block
 constexpr int kPiece = 512;      // local key rows per partial
 
 __device__ __forceinline__ long long natural_key(int r, int i, int n, int c, int layout) {
@@ -49,7 +49,7 @@ __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u 
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
 template <int D>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 2)
     decode_partial_kernel(const DecodeParams p) {
   constexpr int VC = D / 32;   // value columns per lane
   __shared__ __align__(16) float qs[kDecRows][D];
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int r = 0; r < kDecRows; ++r) s[r] = 0.f;
     if (kv) {
       const uint4* krow = reinterpret_cast<const uint4*>(kb + ((static_cast<long long>(b) * p.S + nat) * p.Hkv + g) * D);
-#pragma unroll 4
+#pragma unroll 8
       for (int c8 = 0; c8 < D / 8; ++c8) {
         const uint4 w = __ldg(krow + c8);
         const float kf[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
@@ -158,24 +158,33 @@ __global__ void __launch_bounds__(kDecThreads)
       ps[warp][r][lane] = pr;
     }
     __syncwarp();
-    // ---- P V: lane owns value columns lane*VC .. +VC-1
+    // ---- P V: lane owns value columns lane*VC .. +VC-1; eight value rows
+    // are loaded before any is used so their latencies overlap
     const int nk = min(32, i1 - base);
-    for (int j = 0; j < nk; ++j) {
-      const long long natj = natural_key(shard, base + j, p.n, p.c, p.layout);
-      const __nv_bfloat16* vrow = vb + ((static_cast<long long>(b) * p.S + natj) * p.Hkv + g) * D + lane * VC;
-      float vf[VC];
-      if constexpr (VC == 4) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow));
-        vf[0] = bf16_lo(w.x); vf[1] = bf16_hi(w.x); vf[2] = bf16_lo(w.y); vf[3] = bf16_hi(w.y);
-      } else {
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(vrow));
-        vf[0] = bf16_lo(w); vf[1] = bf16_hi(w);
+    for (int j0 = 0; j0 < nk; j0 += 8) {
+      float vf[8][VC];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = min(j0 + u, nk - 1);
+        const long long natj = natural_key(shard, base + j, p.n, p.c, p.layout);
+        const __nv_bfloat16* vrow = vb + ((static_cast<long long>(b) * p.S + natj) * p.Hkv + g) * D + lane * VC;
+        if constexpr (VC == 4) {
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow));
+          vf[u][0] = bf16_lo(w.x); vf[u][1] = bf16_hi(w.x); vf[u][2] = bf16_lo(w.y); vf[u][3] = bf16_hi(w.y);
+        } else {
+          const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(vrow));
+          vf[u][0] = bf16_lo(w); vf[u][1] = bf16_hi(w);
+        }
       }
 #pragma unroll
-      for (int r = 0; r < kDecRows; ++r) {
-        const float pr = ps[warp][r][j];
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u >= nk) break;
 #pragma unroll
-        for (int c = 0; c < VC; ++c) acc[r][c] = fmaf(pr, vf[c], acc[r][c]);
+        for (int r = 0; r < kDecRows; ++r) {
+          const float pr = ps[warp][r][j0 + u];
+#pragma unroll
+          for (int c = 0; c < VC; ++c) acc[r][c] = fmaf(pr, vf[u][c], acc[r][c]);
+        }
       }
     }
     __syncwarp();

@@ -123,71 +123,104 @@ struct MergeParams {
   const int32_t* out_row;
 };
 
-// One warp per (b, h, row); lanes hold D/32 consecutive columns.
+// One warp per kMergeRows rows of (b, h, s), s fastest; lanes hold D/32
+// consecutive columns of each row.  One online pass over the partials: per
+// partial the warp issues all its rows' loads before using any of them, and
+//   M' = max(M, m_p),  L' = 2^(M - M') L + 2^(m_p - M') l_p,
+//   acc' = 2^(M - M') acc + 2^(m_p - M') o_p            (base-2 units).
+// For a single partial the weights are exactly 1, so out = o / l bit for bit
+// as in the fused kernel's epilogue.
+constexpr int kMergeRows = 4;
+
 template <int D>
-__global__ void merge_kernel(const MergeParams mp) {
+__global__ void __launch_bounds__(256) merge_kernel(const MergeParams mp) {
   constexpr int V = D / 32;   // floats per lane
   const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(mp.B) * mp.Hq * mp.S;
-  if (warp_id >= rows) return;
-  // warp_id enumerates (b, h, s) with s fastest so neighbouring warps read
-  // neighbouring m and l entries.
-  const int s = static_cast<int>(warp_id % mp.S);
-  const int h = static_cast<int>((warp_id / mp.S) % mp.Hq);
-  const int b = static_cast<int>(warp_id / (static_cast<long long>(mp.S) * mp.Hq));
-  const long long si = (static_cast<long long>(b) * mp.Hq + h) * mp.S + s;
-  const long long oi = ((static_cast<long long>(b) * mp.S + s) * mp.Hq + h) * D + lane * V;
-
-  float M = -INFINITY;
-  for (int pi = 0; pi < mp.a.P; ++pi) M = fmaxf(M, __ldg(mp.a.ms[pi] + si));
-  const float Muse = (M == -INFINITY) ? 0.f : M;
-  float L = 0.f;
-  float acc[V];
+  const long long row0 = warp_id * kMergeRows;
+  if (row0 >= rows) return;
+  long long si[kMergeRows], oi[kMergeRows];
+  int bb[kMergeRows], hh[kMergeRows], ss[kMergeRows];
+  bool live[kMergeRows];
 #pragma unroll
-  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  for (int r = 0; r < kMergeRows; ++r) {
+    const long long row = row0 + r;
+    live[r] = row < rows;
+    const long long rr = live[r] ? row : row0;
+    ss[r] = static_cast<int>(rr % mp.S);
+    hh[r] = static_cast<int>((rr / mp.S) % mp.Hq);
+    bb[r] = static_cast<int>(rr / (static_cast<long long>(mp.S) * mp.Hq));
+    si[r] = rr;   // (b, h, s) with s fastest is the m / l layout
+    oi[r] = ((static_cast<long long>(bb[r]) * mp.S + ss[r]) * mp.Hq + hh[r]) * D + lane * V;
+  }
+  float M[kMergeRows], L[kMergeRows], acc[kMergeRows][V];
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+    M[r] = -INFINITY;
+    L[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[r][i] = 0.f;
+  }
   for (int pi = 0; pi < mp.a.P; ++pi) {
-    const float mpv = __ldg(mp.a.ms[pi] + si);
-    const float w = (mpv == -INFINITY) ? 0.f : exp2f(mpv - Muse);
-    L = fmaf(__ldg(mp.a.ls[pi] + si), w, L);
-    const float* op = mp.a.outs[pi] + oi;
-    if constexpr (V == 4) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(op));
-      acc[0] = fmaf(f.x, w, acc[0]);
-      acc[1] = fmaf(f.y, w, acc[1]);
-      acc[2] = fmaf(f.z, w, acc[2]);
-      acc[3] = fmaf(f.w, w, acc[3]);
-    } else {
-      const float2 f = __ldg(reinterpret_cast<const float2*>(op));
-      acc[0] = fmaf(f.x, w, acc[0]);
-      acc[1] = fmaf(f.y, w, acc[1]);
+    const float* mpp = mp.a.ms[pi];
+    const float* lpp = mp.a.ls[pi];
+    const float* opp = mp.a.outs[pi];
+    float mv[kMergeRows], lv[kMergeRows], ov[kMergeRows][V];
+#pragma unroll
+    for (int r = 0; r < kMergeRows; ++r) {
+      mv[r] = __ldg(mpp + si[r]);
+      lv[r] = __ldg(lpp + si[r]);
+      if constexpr (V == 4) {
+        const float4 f = __ldcs(reinterpret_cast<const float4*>(opp + oi[r]));
+        ov[r][0] = f.x; ov[r][1] = f.y; ov[r][2] = f.z; ov[r][3] = f.w;
+      } else {
+        const float2 f = __ldcs(reinterpret_cast<const float2*>(opp + oi[r]));
+        ov[r][0] = f.x; ov[r][1] = f.y;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kMergeRows; ++r) {
+      if (mv[r] == -INFINITY) continue;   // an empty partial adds nothing
+      const float Mn = fmaxf(M[r], mv[r]);
+      const float alpha = (M[r] == Mn) ? 1.f : exp2f(M[r] - Mn);
+      const float w = (mv[r] == Mn) ? 1.f : exp2f(mv[r] - Mn);
+      L[r] = fmaf(lv[r], w, L[r] * alpha);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[r][i] = fmaf(ov[r][i], w, acc[r][i] * alpha);
+      M[r] = Mn;
     }
   }
-  const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  const int orow = (mp.out_row != nullptr) ? mp.out_row[s] : s;
-  const long long od = ((static_cast<long long>(b) * mp.S_out + orow) * mp.Hq + h) * D + lane * V;
-  if (mp.out_dtype == RA_F32) {
-    float* o = static_cast<float*>(mp.out) + od;
-    if constexpr (V == 4)
-      *reinterpret_cast<float4*>(o) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    else
-      *reinterpret_cast<float2*>(o) = make_float2(acc[0] * inv, acc[1] * inv);
-  } else {
-    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(mp.out) + od;
-    if constexpr (V == 4) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-      uint2 w;
-      w.x = *reinterpret_cast<uint32_t*>(&lo);
-      w.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(o) = w;
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+    if (!live[r]) continue;
+    const float inv = (L[r] > 0.f) ? 1.f / L[r] : 0.f;
+    const int orow = (mp.out_row != nullptr) ? mp.out_row[ss[r]] : ss[r];
+    const long long od = ((static_cast<long long>(bb[r]) * mp.S_out + orow) * mp.Hq + hh[r]) * D + lane * V;
+    if (mp.out_dtype == RA_F32) {
+      float* o = static_cast<float*>(mp.out) + od;
+      if constexpr (V == 4)
+        *reinterpret_cast<float4*>(o) =
+            make_float4(acc[r][0] * inv, acc[r][1] * inv, acc[r][2] * inv, acc[r][3] * inv);
+      else
+        *reinterpret_cast<float2*>(o) = make_float2(acc[r][0] * inv, acc[r][1] * inv);
     } else {
-      *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(mp.out) + od;
+      if constexpr (V == 4) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[r][0] * inv, acc[r][1] * inv);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[r][2] * inv, acc[r][3] * inv);
+        uint2 w;
+        w.x = *reinterpret_cast<uint32_t*>(&lo);
+        w.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(o) = w;
+      } else {
+        *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc[r][0] * inv, acc[r][1] * inv);
+      }
     }
+    if (lane == 0 && mp.lse != nullptr)
+      mp.lse[(static_cast<long long>(bb[r]) * mp.Hq + hh[r]) * mp.S_out + orow] =
+          (L[r] > 0.f) ? (M[r] + log2f(L[r])) * 0.69314718055994531f : -INFINITY;
   }
-  if (lane == 0 && mp.lse != nullptr)
-    mp.lse[(static_cast<long long>(b) * mp.Hq + h) * mp.S_out + orow] =
-        (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 int grid_for(long long work, int threads) {
@@ -266,7 +299,8 @@ int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype,
   mp.lse = lse;
   mp.out_row = out_row;
   const int threads = 256;
-  const long long blocks = (rows * 32 + threads - 1) / threads;
+  const long long warps = (rows + kMergeRows - 1) / kMergeRows;
+  const long long blocks = (warps * 32 + threads - 1) / threads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 128)
     merge_kernel<128><<<static_cast<unsigned>(blocks), threads, 0, s>>>(mp);
