@@ -98,19 +98,21 @@ struct Abort {
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, Abort ab,
                                            unsigned int code) {
   const uint64_t t0 = ptx::global_timer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 4; ++i)
-      if (ptx::mbar_try_wait(bar, parity)) return true;
+  for (uint32_t n = 1;; ++n) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*ab.flag) return false;
-    if (*reinterpret_cast<volatile unsigned int*>(ab.err) != 0) {
-      *ab.flag = 1;   // another block already gave up: stop early
-      return false;
-    }
-    if (ptx::global_timer_ns() - t0 > kWaitTimeoutNs) {
-      *ab.flag = 1;
-      atomicOr(ab.err, code);
-      return false;
+    // The device-wide error word and the clock are read only now and then:
+    // a global load in the loop would delay noticing the phase change.
+    if ((n & 255u) == 0) {
+      if (*reinterpret_cast<volatile unsigned int*>(ab.err) != 0) {
+        *ab.flag = 1;   // another block already gave up: stop early
+        return false;
+      }
+      if (ptx::global_timer_ns() - t0 > kWaitTimeoutNs) {
+        *ab.flag = 1;
+        atomicOr(ab.err, code);
+        return false;
+      }
     }
   }
 }
@@ -187,6 +189,35 @@ __device__ __forceinline__ KTile k_tile(const AttnParams& p, int src, int kt, co
     k.mx = r.y;
   } else {
     warp_minmax(p.k_pos + static_cast<long long>(src) * p.n_k + start, k.valid, lane, k.mn, k.mx);
+  }
+  k.skip = p.causal ? (k.mn > q.mx_all) : (q.valid[0] + q.valid[1] == 0);
+  return k;
+}
+
+// Key tile kt of shard `src` as seen by a single thread: the staged ranges,
+// else the ranges in global memory, else a serial reduction of the positions.
+__device__ __forceinline__ KTile k_tile_1(const AttnParams& p, int src, int kt, const QTiles& q,
+                                          int ktiles, const int2* rs) {
+  KTile k;
+  const int start = kt * kTile;
+  k.valid = min(kTile, p.n_k - start);
+  if (rs != nullptr) {
+    const int2 r = rs[kt];
+    k.mn = r.x;
+    k.mx = r.y;
+  } else if (p.k_ranges != nullptr) {
+    const int2 r = p.k_ranges[static_cast<long long>(src) * ktiles + kt];
+    k.mn = r.x;
+    k.mx = r.y;
+  } else {
+    const int32_t* pos = p.k_pos + static_cast<long long>(src) * p.n_k + start;
+    k.mn = INT_MAX;
+    k.mx = INT_MIN;
+    for (int i = 0; i < k.valid; ++i) {
+      const int v = __ldg(pos + i);
+      k.mn = min(k.mn, v);
+      k.mx = max(k.mx, v);
+    }
   }
   k.skip = p.causal ? (k.mn > q.mx_all) : (q.valid[0] + q.valid[1] == 0);
   return k;
@@ -346,60 +377,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ===================== tensor-core issue ============================
-    constexpr uint32_t idS = ptx::idesc_bf16_f32(128, 128, false);
-    constexpr uint32_t idPV = ptx::idesc_bf16_f32(128, D, true);
-    bool ok = true;
-    bool issued_any = false;
-    if (lane == 0) ok = wait_bar(bar(L::bQ), 0, ab, kErrTimeoutQ);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-
-    auto issue_S = [&](int hh, int ks) {
-      const uint32_t qa = sbase + L::kQ + hh * L::kTileBytes;
-      const uint32_t ka = sbase + L::kK + ks * L::kTileBytes;
+    // One thread runs this loop: tcgen05.mma issue holds the issuing thread
+    // until the tensor core takes the instruction, so everything between two
+    // batches is kept short.
+    if (lane == 0) {
+      constexpr uint32_t idS = ptx::idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idPV = ptx::idesc_bf16_f32(128, D, true);
+      bool ok = wait_bar(bar(L::bQ), 0, ab, kErrTimeoutQ);
+      bool issued_any = false;
+      // Shared-memory descriptors of the first Q tile / K stage / V stage;
+      // the others differ only in the 16-byte address field (bits 0-13).
+      const uint64_t dQ = ptx::smem_desc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t dK = ptx::smem_desc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t dV = ptx::smem_desc_sw128(sbase + L::kV, L::kBoxBytes, 1024);
+      auto issue_S = [&](int hh, int ks) {
+        const uint64_t qd = dQ + static_cast<uint64_t>((hh * L::kTileBytes) >> 4);
+        const uint64_t kd = dK + static_cast<uint64_t>((ks * L::kTileBytes) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * L::kBoxBytes + (kk % 4) * 32;
-        ptx::tc_mma_ss(tmem + col_S(hh), ptx::smem_desc_sw128(qa + off, 16, 1024),
-                       ptx::smem_desc_sw128(ka + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
-      }
-    };
-    auto issue_PV = [&](int hh, int vs) {
-      const uint32_t va = sbase + L::kV + vs * L::kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        ptx::tc_mma_ts(tmem + col_O(hh), tmem + col_S(hh) + kk * 8,
-                       ptx::smem_desc_sw128(va + kk * 16 * 128, L::kBoxBytes, 1024), idPV, 1u);
-      }
-    };
-
-    uint32_t j = 0;
-    for (int t = p.t_begin; t < p.t_end && ok; ++t) {
-      const int src = step_src(p, rank, t);
-      const int2* rs = step_ranges(t);
-      unsigned long long nfull = 0, npart = 0, nskip = 0;
-      for (int kt = 0; kt < ktiles; ++kt) {
-        const KTile k = k_tile(p, src, kt, qt, lane, rs);
-        if (p.work != nullptr) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            if (qt.valid[hh] == 0) continue;
-            if (!p.causal || k.mx <= qt.mn[hh]) ++nfull;
-            else if (k.mn > qt.mx[hh]) ++nskip;
-            else ++npart;
-          }
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o = static_cast<uint64_t>(((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4);
+          ptx::tc_mma_ss(tmem + col_S(hh), qd + o, kd + o, idS, kk > 0 ? 1u : 0u);
         }
-        if (k.skip) continue;
-        if (lane == 0) {
+      };
+      auto issue_PV = [&](int hh, int vs) {
+        const uint64_t vd = dV + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          ptx::tc_mma_ts(tmem + col_O(hh), tmem + col_S(hh) + kk * 8,
+                         vd + static_cast<uint64_t>((kk * 16 * 128) >> 4), idPV, 1u);
+      };
+
+      uint32_t j = 0;
+      for (int t = p.t_begin; t < p.t_end && ok; ++t) {
+        const int src = step_src(p, rank, t);
+        const int2* rs = step_ranges(t);
+        unsigned long long nfull = 0, npart = 0, nskip = 0;
+        for (int kt = 0; kt < ktiles; ++kt) {
+          const KTile k = k_tile_1(p, src, kt, qt, ktiles, rs);
+          if (p.work != nullptr) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              if (qt.valid[hh] == 0) continue;
+              if (!p.causal || k.mx <= qt.mn[hh]) ++nfull;
+              else if (k.mn > qt.mx[hh]) ++nskip;
+              else ++npart;
+            }
+          }
+          if (k.skip) continue;
           const int ks = static_cast<int>(j % L::KST);
           ok = wait_bar(bar(L::bKFull + ks), (j / L::KST) & 1u, ab, kErrTimeoutK);
-          if (ok) ptx::tc_fence_after_sync();
-          if (ok && j == 0) {
+          if (!ok) break;
+          ptx::tc_fence_after_sync();
+          if (j == 0) {
             for (int hh = 0; hh < 2; ++hh) {
               issue_S(hh, ks);
               ptx::tc_commit(bar(L::bSFull + hh));
             }
             issued_any = true;
-          } else if (ok) {
+          } else {
             const uint32_t jp = j - 1;
             const int vs = static_cast<int>(jp % L::VST);
             ok = wait_bar(bar(L::bVFull + vs), (jp / L::VST) & 1u, ab, kErrTimeoutV);
@@ -413,20 +448,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok) ptx::tc_commit(bar(L::bVEmpty + vs));
           }
-          if (ok) ptx::tc_commit(bar(L::bKEmpty + ks));
+          if (!ok) break;
+          ptx::tc_commit(bar(L::bKEmpty + ks));
+          ++j;
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        ++j;
+        if (p.work != nullptr && ok) {
+          ra_work* w = p.work + static_cast<long long>(rank) * p.c + t;
+          atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_full), nfull);
+          atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_partial), npart);
+          atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_skipped), nskip);
+        }
       }
-      if (p.work != nullptr && lane == 0 && ok) {
-        ra_work* w = p.work + static_cast<long long>(rank) * p.c + t;
-        atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_full), nfull);
-        atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_partial), npart);
-        atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_skipped), nskip);
-      }
-    }
-    if (lane == 0) {
       if (ok && j > 0) {
         const uint32_t jp = j - 1;
         const int vs = static_cast<int>(jp % L::VST);
@@ -587,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
         const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
         uint64_t acc = ptx::f2_pack(0.f, 0.f);
+        uint64_t acc1 = ptx::f2_pack(0.f, 0.f);
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t sh[64];
@@ -608,14 +641,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::f2_unpack(x, x0, x1);
               const float e0 = ptx::ex2(x0);
               const float e1 = ptx::ex2(x1);
-              acc = ptx::f2_add(acc, ptx::f2_pack(e0, e1));
+              if (i & 1) acc1 = ptx::f2_add(acc1, ptx::f2_pack(e0, e1));
+              else acc = ptx::f2_add(acc, ptx::f2_pack(e0, e1));
               pk[i] = ptx::pack_bf16x2(e0, e1);
             }
             ptx::tmem_st16(tS + half * 32 + cc * 16, pk);
           }
         }
         float sm0, sm1;
-        ptx::f2_unpack(acc, sm0, sm1);
+        ptx::f2_unpack(ptx::f2_add(acc, acc1), sm0, sm1);
         const float sum = sm0 + sm1;
         l_run = l_run * alpha + sum;
         m_run = m_new;

@@ -123,8 +123,10 @@ struct MergeParams {
   const int32_t* out_row;
 };
 
-// One warp per kMergeRows rows of (b, h, s), s fastest; lanes hold D/32
-// consecutive columns of each row.  One online pass over the partials: per
+// One warp per kMergeRows rows of (b, s, h), h fastest -- the order of the
+// partial outputs in memory, so a warp reads one contiguous stretch and
+// neighbouring warps the next ones; lanes hold D/32 consecutive columns of
+// each row.  One online pass over the partials: per
 // partial the warp issues all its rows' loads before using any of them, and
 //   M' = max(M, m_p),  L' = 2^(M - M') L + 2^(m_p - M') l_p,
 //   acc' = 2^(M - M') acc + 2^(m_p - M') o_p            (base-2 units).
@@ -148,11 +150,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams mp) {
     const long long row = row0 + r;
     live[r] = row < rows;
     const long long rr = live[r] ? row : row0;
-    ss[r] = static_cast<int>(rr % mp.S);
-    hh[r] = static_cast<int>((rr / mp.S) % mp.Hq);
+    hh[r] = static_cast<int>(rr % mp.Hq);
+    ss[r] = static_cast<int>((rr / mp.Hq) % mp.S);
     bb[r] = static_cast<int>(rr / (static_cast<long long>(mp.S) * mp.Hq));
-    si[r] = rr;   // (b, h, s) with s fastest is the m / l layout
-    oi[r] = ((static_cast<long long>(bb[r]) * mp.S + ss[r]) * mp.Hq + hh[r]) * D + lane * V;
+    si[r] = (static_cast<long long>(bb[r]) * mp.Hq + hh[r]) * mp.S + ss[r];
+    oi[r] = rr * D + lane * V;   // o is [B, S, Hq, D]: rows in this order are consecutive
   }
   float M[kMergeRows], L[kMergeRows], acc[kMergeRows][V];
 #pragma unroll
