@@ -448,7 +448,7 @@ ra_status ra_ring_forward(const void* q, const void* k, const void* v, ra_shape 
 }
 
 namespace {
-// Partials of a decode call: P = c * pieces per shard.
+// Partials of a decode call: one per block over the c * pieces-per-shard pieces.
 struct DecodeWs {
   int P;
   size_t o, m, l, total;
@@ -457,7 +457,7 @@ struct DecodeWs {
 DecodeWs decode_ws(const ra_shape& s, int c) {
   DecodeWs w;
   const int n = s.Sk / c;
-  w.P = c * ra::decode_pieces_per_shard(n);
+  w.P = ra::decode_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, c * ra::decode_pieces_per_shard(n));
   const size_t P = static_cast<size_t>(w.P), B = static_cast<size_t>(s.B), R = static_cast<size_t>(s.Sq);
   size_t off = 0;
   w.o = off;  off = round_up(off + P * B * R * s.Hq * s.D * sizeof(float));

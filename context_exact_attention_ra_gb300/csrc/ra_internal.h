@@ -66,7 +66,8 @@ struct DecodeParams {
   const int32_t* q_pos;        // [R] their global positions
   const void* k;               // [B, S, Hkv, D] bf16, natural order
   const void* v;
-  int pieces_per_shard, P;     // P = c * pieces_per_shard partials
+  int pieces_per_shard;        // shard-local pieces of the key range
+  int P;                       // partials per query row (blocks over the c * pieces_per_shard pieces)
   float* part_o;               // [P, B, R, Hq, D]
   float* part_m;               // [P, B, Hq, R] (base-2 units)
   float* part_l;
@@ -109,6 +110,8 @@ int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype,
 int launch_zero(void* ptr, size_t bytes, void* stream);
 int launch_decode(const DecodeParams& p, void* stream);
 int decode_pieces_per_shard(int n);
+// Number of partial states (blocks per batch, key/value head and row block).
+int decode_partials(int B, int Hkv, int G, int R, int pieces);
 unsigned int* device_error_word(int* cuda_err);
 // Name of the host step that produced the last launcher error (thread-local).
 const char*& launch_stage();
