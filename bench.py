@@ -40,7 +40,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="s128k")
     ap.add_argument("--layout", default=None)
-    ap.add_argument("--mode", default="fused", choices=["fused", "per_step"])
+    ap.add_argument("--mode", default="fused", choices=["fused", "per_step", "allgather"],
+                    help="fused ring (one launch), per-step launches + merge, or one step over all-gathered keys")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -243,7 +244,11 @@ def run_ours(args, rank, world, local):
         flush.zero_()
         step()
     ra.device_error()
-    launches_per_step = 2 + (1 if md == ra.MODE_FUSED else w.c + 2)
+    # ra_ring_prepare: pack, tile ranges, heavy-first block order (every
+    # workload here has more than one query block); ra_ring_attend: one
+    # launch, or state init + c steps + merge in per-step mode
+    prep_launches = 3
+    launches_per_step = prep_launches + (w.c + 2 if md == ra.MODE_PER_STEP else 1)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -277,7 +282,9 @@ def run_ours(args, rank, world, local):
     peak = float(peaks["bf16_tflops"])
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": kernel_traffic("attn_tc_sm103.cu") if md == ra.MODE_FUSED else None,
-            "kernel": "attn_fwd_tc_kernel<128>" if md == ra.MODE_FUSED else "attend (per-step launches + merge)",
+            "kernel": {ra.MODE_FUSED: "attn_fwd_tc_kernel<128>",
+                       ra.MODE_ALLGATHER: "attn_fwd_tc_kernel<128> (one step over the gathered keys)"}.get(
+                           md, "attend (per-step launches + merge)"),
             "peak_source": f"{peak_kind} bf16_tflops (burst)",
             "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
             "frac_of_nominal_dense": achieved / NOMINAL_BF16_DENSE_TFLOPS}

@@ -132,10 +132,10 @@ struct MergeParams {
 //   acc' = 2^(M - M') acc + 2^(m_p - M') o_p            (base-2 units).
 // For a single partial the weights are exactly 1, so out = o / l bit for bit
 // as in the fused kernel's epilogue.
-constexpr int kMergeRows = 4;
+constexpr int kMergeRows = 2;
 
 template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeParams mp) {
+__global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams mp) {
   constexpr int V = D / 32;   // floats per lane
   const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -145,16 +145,27 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams mp) {
   long long si[kMergeRows], oi[kMergeRows];
   int bb[kMergeRows], hh[kMergeRows], ss[kMergeRows];
   bool live[kMergeRows];
+  // (b, s, h) of the first row by division, of the others by stepping h
+  const long long q0 = row0 / mp.Hq;
+  int h = static_cast<int>(row0 - q0 * mp.Hq);
+  int sidx = static_cast<int>(q0 % mp.S);
+  int bidx = static_cast<int>(q0 / mp.S);
 #pragma unroll
   for (int r = 0; r < kMergeRows; ++r) {
     const long long row = row0 + r;
     live[r] = row < rows;
-    const long long rr = live[r] ? row : row0;
-    hh[r] = static_cast<int>(rr % mp.Hq);
-    ss[r] = static_cast<int>((rr / mp.Hq) % mp.S);
-    bb[r] = static_cast<int>(rr / (static_cast<long long>(mp.S) * mp.Hq));
+    hh[r] = live[r] ? h : hh[0];
+    ss[r] = live[r] ? sidx : ss[0];
+    bb[r] = live[r] ? bidx : bb[0];
     si[r] = (static_cast<long long>(bb[r]) * mp.Hq + hh[r]) * mp.S + ss[r];
-    oi[r] = rr * D + lane * V;   // o is [B, S, Hq, D]: rows in this order are consecutive
+    oi[r] = (live[r] ? row : row0) * D + lane * V;   // o is [B, S, Hq, D]: rows in this order are consecutive
+    if (++h == mp.Hq) {
+      h = 0;
+      if (++sidx == mp.S) {
+        sidx = 0;
+        ++bidx;
+      }
+    }
   }
   float M[kMergeRows], L[kMergeRows], acc[kMergeRows][V];
 #pragma unroll
@@ -222,6 +233,72 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams mp) {
     if (lane == 0 && mp.lse != nullptr)
       mp.lse[(static_cast<long long>(bb[r]) * mp.Hq + hh[r]) * mp.S_out + orow] =
           (L[r] > 0.f) ? (M[r] + log2f(L[r])) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+// One partial (the per-step mode's last step): out = o / l and
+// lse = m + log2 l, with m in base-2 units -- the fused kernel's epilogue
+// arithmetic, so both modes agree bit for bit.  Each thread owns one 16-byte
+// slice of kFinRows consecutive rows ((b, s, h) with h fastest, the order of o
+// in memory) and issues all their loads before using any.
+constexpr int kFinRows = 4;
+
+template <int D>
+__global__ void __launch_bounds__(256) finalize_kernel(const MergeParams mp) {
+  constexpr int C = D / 4;   // float4 slices per row
+  const long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long rows = static_cast<long long>(mp.B) * mp.Hq * mp.S;
+  const int c4 = static_cast<int>(t % C);
+  const long long row0 = (t / C) * kFinRows;
+  if (row0 >= rows) return;
+  const float* o = mp.a.outs[0];
+  const float* m = mp.a.ms[0];
+  const float* l = mp.a.ls[0];
+  const long long q0 = row0 / mp.Hq;
+  int h = static_cast<int>(row0 - q0 * mp.Hq);
+  int sidx = static_cast<int>(q0 % mp.S);
+  int bidx = static_cast<int>(q0 / mp.S);
+  float4 ov[kFinRows];
+  float mv[kFinRows], lv[kFinRows];
+  int hh[kFinRows], ss[kFinRows], bb[kFinRows];
+#pragma unroll
+  for (int r = 0; r < kFinRows; ++r) {
+    const bool live = row0 + r < rows;
+    hh[r] = h;
+    ss[r] = sidx;
+    bb[r] = bidx;
+    const long long si = (static_cast<long long>(bidx) * mp.Hq + h) * mp.S + sidx;
+    ov[r] = live ? __ldcs(reinterpret_cast<const float4*>(o + (row0 + r) * D) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    mv[r] = live ? m[si] : 0.f;
+    lv[r] = live ? l[si] : 0.f;
+    if (++h == mp.Hq) {
+      h = 0;
+      if (++sidx == mp.S) {
+        sidx = 0;
+        ++bidx;
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kFinRows; ++r) {
+    if (row0 + r >= rows) break;
+    const float inv = (lv[r] > 0.f) ? 1.f / lv[r] : 0.f;
+    const int orow = (mp.out_row != nullptr) ? mp.out_row[ss[r]] : ss[r];
+    const long long od = ((static_cast<long long>(bb[r]) * mp.S_out + orow) * mp.Hq + hh[r]) * D + c4 * 4;
+    if (mp.out_dtype == RA_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(mp.out) + od) =
+          make_float4(ov[r].x * inv, ov[r].y * inv, ov[r].z * inv, ov[r].w * inv);
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(ov[r].x * inv, ov[r].y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(ov[r].z * inv, ov[r].w * inv);
+      uint2 w;
+      w.x = *reinterpret_cast<uint32_t*>(&lo);
+      w.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(mp.out) + od) = w;
+    }
+    if (c4 == 0 && mp.lse != nullptr)
+      mp.lse[(static_cast<long long>(bb[r]) * mp.Hq + hh[r]) * mp.S_out + orow] =
+          (lv[r] > 0.f) ? (mv[r] + log2f(lv[r])) * 0.69314718055994531f : -INFINITY;
   }
 }
 
@@ -301,9 +378,20 @@ int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype,
   mp.lse = lse;
   mp.out_row = out_row;
   const int threads = 256;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a.P == 1) {
+    const long long nthreads = (rows + kFinRows - 1) / kFinRows * (D / 4);
+    const long long fblocks = (nthreads + threads - 1) / threads;
+    if (D == 128)
+      finalize_kernel<128><<<static_cast<unsigned>(fblocks), threads, 0, s>>>(mp);
+    else if (D == 64)
+      finalize_kernel<64><<<static_cast<unsigned>(fblocks), threads, 0, s>>>(mp);
+    else
+      return static_cast<int>(cudaErrorInvalidValue);
+    return static_cast<int>(cudaGetLastError());
+  }
   const long long warps = (rows + kMergeRows - 1) / kMergeRows;
   const long long blocks = (warps * 32 + threads - 1) / threads;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 128)
     merge_kernel<128><<<static_cast<unsigned>(blocks), threads, 0, s>>>(mp);
   else if (D == 64)
