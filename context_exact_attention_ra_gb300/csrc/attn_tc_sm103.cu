@@ -545,7 +545,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // visibility of each key column (partial tiles only), before S is loaded
         uint32_t bits[4] = {~0u, ~0u, ~0u, ~0u};
         unsigned int nvis = static_cast<unsigned int>(k.valid);
-        if (masked) {
+        if (masked && p.k_sorted) {
+          // positions increase inside the tile: the visible keys are the prefix
+          // of those at or before this row's position (binary search)
+          int cnt = k.valid;
+          if (p.causal) {
+            cnt = 0;
+#pragma unroll
+            for (int step = 128; step > 0; step >>= 1)
+              if (cnt + step <= k.valid && __ldg(kp + cnt + step - 1) <= qpos) cnt += step;
+          }
+          nvis = static_cast<unsigned int>(cnt);
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            bits[w] = cnt >= 32 * (w + 1) ? ~0u : (cnt > 32 * w ? (1u << (cnt - 32 * w)) - 1u : 0u);
+        } else if (masked) {
           nvis = 0;
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {

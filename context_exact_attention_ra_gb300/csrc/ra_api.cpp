@@ -277,6 +277,7 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
   const int S = shp.Sq;
   const int n = S / c;
   AttnParams p = base_params(shp, c, n, n, causal);
+  p.k_sorted = 1;   // shard rows are in increasing position in every layout
   p.q_pos = at<int32_t>(workspace, w.pos);
   p.k_pos = p.q_pos;
   p.k_ranges = at<int2>(workspace, w.ranges);
@@ -312,7 +313,10 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
     p.finalize = 1;
     // per-rank key-tile ranges coincide with the gathered buffer's tiles only
     // when shards are whole tiles; otherwise the kernel reduces them itself
-    if (n % ra::kTile != 0) p.k_ranges = nullptr;
+    if (n % ra::kTile != 0) {
+      p.k_ranges = nullptr;
+      p.k_sorted = 0;   // a tile may span two shards
+    }
     return launch_attn(p, shp, S, S, stream);
   }
   // Per-step: state in the workspace, one launch per ring step, then out / l.
@@ -560,6 +564,7 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
   char* vbuf[2] = {at<char>(workspace, w.vp), at<char>(workspace, w.total + round_up(kvb))};
 
   AttnParams p = base_params(shp, c, n, n, causal);
+  p.k_sorted = 1;   // shard rows are in increasing position in every layout
   p.q_pos = at<int32_t>(workspace, w.pos);
   p.k_pos = p.q_pos;
   p.k_ranges = at<int2>(workspace, w.ranges);

@@ -26,6 +26,8 @@ struct AttnParams {
   int n_q, n_k;                // rows per rank
   int t_begin, t_end;          // ring steps handled by this launch
   int kv_all;                  // 1: one step over all c*n_k key rows (all-gather), no ring
+  int k_sorted;                // 1: key positions increase inside every key tile (the library's
+                               //    own layouts), so a row's visible keys in a tile are a prefix
   int kv_by_holder;            // 1: the block held at a step sits in the holder's slot of k, v
                                //    (rows rank*n_k ..), its positions are the source's
   int q_blocks_per_rank;       // ceil(n_q / rows per block)
