@@ -31,6 +31,7 @@ MODE_FUSED, MODE_PER_STEP, MODE_ALLGATHER = 0, 1, 2
 LAYOUTS = {"contiguous": CONTIGUOUS, "zigzag": ZIGZAG, "striped": STRIPED}
 MODES = {"fused": MODE_FUSED, "per_step": MODE_PER_STEP, "allgather": MODE_ALLGATHER}
 MERGE_MAX_PARTIALS = 64
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
 
 
 class RaError(RuntimeError):
@@ -100,6 +101,7 @@ _SIGS = {
     "ra_work_expected": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(Work)]),
     "ra_device_error": (ctypes.c_int, [_P]),
+    "ra_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
     "ra_ring_forward_noalloc": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
 }
@@ -423,3 +425,9 @@ def ring_forward_noalloc(q, k, v, c, layout="zigzag", causal=True, mode="fused",
 def device_error(stream=None):
     """Synchronise and read/clear the device error word; raises on a timeout."""
     _check(lib().ra_device_error(_stream(stream)), "device wait")
+
+
+def selftest_wait_timeout(limit_us=20000, stream=None):
+    """Run the device-timeout self-test: a bounded wait on a barrier that
+    nothing arrives on.  Returns the status (TIMEOUT when the path works)."""
+    return int(lib().ra_selftest_wait_timeout(int(limit_us), _stream(stream)))

@@ -43,6 +43,7 @@
 #include <mutex>
 
 #include "ra_internal.h"
+#include "ra_wait.cuh"
 #include "sm103_ptx.cuh"
 
 namespace ra {
@@ -53,8 +54,6 @@ constexpr int kWarpV = 9;
 constexpr int kWarpMma = 10;
 constexpr int kThreads = 11 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitTimeoutNs = 4000000000ull;
-constexpr uint64_t kDrainTimeoutNs = 200000000ull;
 
 template <int D>
 struct Smem {
@@ -89,49 +88,6 @@ struct Smem {
 // Tensor-memory column of each accumulator.
 __device__ __forceinline__ uint32_t col_S(int h) { return static_cast<uint32_t>(h * 128); }
 __device__ __forceinline__ uint32_t col_O(int h) { return static_cast<uint32_t>(256 + h * 128); }
-
-struct Abort {
-  volatile int* flag;
-  unsigned int* err;
-};
-
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, Abort ab,
-                                           unsigned int code) {
-  const uint64_t t0 = ptx::global_timer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*ab.flag) return false;
-    // The device-wide error word and the clock are read only now and then:
-    // a global load in the loop would delay noticing the phase change.
-    if ((n & 255u) == 0) {
-      if (*reinterpret_cast<volatile unsigned int*>(ab.err) != 0) {
-        *ab.flag = 1;   // another block already gave up: stop early
-        return false;
-      }
-      if (ptx::global_timer_ns() - t0 > kWaitTimeoutNs) {
-        *ab.flag = 1;
-        atomicOr(ab.err, code);
-        return false;
-      }
-    }
-  }
-}
-
-// Bounded wait for the phase of `bar` with the given parity.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Abort ab,
-                                         unsigned int code) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_bar_slow(bar, parity, ab, code);
-}
-
-// Wait used on the abort path: ignores the abort flag, shorter limit.
-__device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = ptx::global_timer_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::global_timer_ns() - t0 > kDrainTimeoutNs) return false;
-  }
-  return true;
-}
 
 // Warp-cooperative min and max of count >= 0 positions (INT_MAX / INT_MIN if empty).
 __device__ __forceinline__ void warp_minmax(const int32_t* pos, int count, int lane, int& mn,

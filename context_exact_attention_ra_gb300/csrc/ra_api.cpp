@@ -360,6 +360,19 @@ ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const voi
   return RA_OK;
 }
 
+ra_status ra_selftest_wait_timeout(uint32_t limit_us, ra_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return RA_ERR_INVALID;
+  int err = 0;
+  unsigned int* ew = ra::device_error_word(&err);
+  if (ew == nullptr) return cuda_fail(err, "device error word lookup");
+  unsigned int pending = 0;
+  int e = ra::read_and_clear_error(stream, &pending);   // start from a clear word
+  if (e) return cuda_fail(e, "device error word read");
+  e = ra::launch_selftest_timeout(ew, static_cast<uint64_t>(limit_us) * 1000u, stream);
+  if (e) return cuda_fail(e, ra::launch_stage());
+  return ra_device_error(stream);
+}
+
 ra_status ra_device_error(ra_stream_t stream) {
   unsigned int v = 0;
   int e = ra::read_and_clear_error(stream, &v);

@@ -88,6 +88,7 @@ enum : unsigned int {
   kErrTimeoutO = 1u << 5,
   kErrTimeoutDrain = 1u << 6,
   kErrTimeoutEmpty = 1u << 7,
+  kErrSelfTest = 1u << 8,       // the self-test's deliberately unsatisfied wait
 };
 
 // ---- launchers (return a cudaError_t as int; 0 = success) -------------
@@ -118,6 +119,7 @@ unsigned int* device_error_word(int* cuda_err);
 // Name of the host step that produced the last launcher error (thread-local).
 const char*& launch_stage();
 int read_and_clear_error(void* stream, unsigned int* value);
+int launch_selftest_timeout(unsigned int* err, uint64_t limit_ns, void* stream);
 
 // ---- host scheduler (ra_sched.cpp) ------------------------------------
 void shard_positions(int S, int c, int layout, int32_t* pos);

@@ -306,6 +306,17 @@ ra_status ra_work_expected(int S, int c, int layout, int causal, ra_work* out);
  * RA_OK, RA_ERR_TIMEOUT or RA_ERR_CUDA. */
 ra_status ra_device_error(ra_stream_t stream);
 
+/* Self-test of the device-timeout path (the pages have no counterpart: they
+ * assume the ring completes).  Clears any pending device error, then runs one
+ * block that waits, through the same bounded wait as the attention kernels, on
+ * a barrier that nothing ever arrives on.  The wait gives up after about
+ * limit_us microseconds (1 .. 1000000; the check runs every 256 polls, so the
+ * real time can be longer), sets its bit in the device error word and the
+ * kernel returns.  Returns RA_ERR_TIMEOUT when the path works as designed (the
+ * error word is cleared again), RA_ERR_INVALID for a bad limit, RA_ERR_CUDA if
+ * a CUDA call fails.  The device stays usable afterwards. */
+ra_status ra_selftest_wait_timeout(uint32_t limit_us, ra_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

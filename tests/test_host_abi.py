@@ -135,3 +135,8 @@ def test_expected_work_at_c16_reproduces_the_plate():
     z = ra.work_expected(S, c, "zigzag", True)
     zr = [sum(z[i][t][0] for t in range(c)) for i in range(c)]
     assert len(set(zr)) == 1
+
+
+def test_selftest_rejects_a_bad_limit_before_any_launch(lib):
+    assert lib.ra_selftest_wait_timeout(ctypes.c_uint32(0), ctypes.c_void_p(0)) == -1
+    assert lib.ra_selftest_wait_timeout(ctypes.c_uint32(2000000), ctypes.c_void_p(0)) == -1
