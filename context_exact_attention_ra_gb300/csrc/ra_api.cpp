@@ -10,8 +10,26 @@
 #include <cstring>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ra.h"
 #include "ra_internal.h"
+
+namespace {
+// NVTX range for profilers (a no-op unless a tool is attached).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+// Name of ring step t for the per-step ranges (the tool reads it during the push).
+const char* step_name(int t) {
+  thread_local char name[32];
+  std::snprintf(name, sizeof(name), "ring step %d", t);
+  return name;
+}
+}  // namespace
 
 namespace {
 
@@ -231,6 +249,7 @@ size_t ra_ring_forward_workspace_size(ra_shape shp, int c, int layout, int mode)
 
 ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape shp, int c,
                           int layout, void* workspace, size_t ws_bytes, ra_stream_t stream) {
+  const Range range("ra_ring_prepare");
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
   if (shp.B == 0 || shp.Sq == 0) return RA_OK;
@@ -260,6 +279,7 @@ ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape 
 ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, int out_dtype,
                          void* out, float* lse, void* workspace, size_t ws_bytes, int count_work,
                          ra_stream_t stream) {
+  const Range range("ra_ring_attend");
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
   if (!mode_ok(mode)) return RA_ERR_INVALID;
@@ -329,6 +349,7 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
   int e = ra::launch_state_init(shp.B, S, shp.Hq, shp.D, p.o_state, p.m_state, p.l_state, stream);
   if (e) return cuda_fail(e, ra::launch_stage());
   for (int t = 0; t < c; ++t) {
+    const Range step(step_name(t));
     p.t_begin = t;
     p.t_end = t + 1;
     st = launch_attn(p, shp, S, S, stream);
@@ -502,6 +523,7 @@ size_t ra_decode_workspace_size(ra_shape shp, int c, int layout) {
 ra_status ra_decode_forward(const void* q, const int32_t* q_pos, const void* k, const void* v,
                             ra_shape shp, int c, int layout, int causal, int out_dtype, void* out,
                             float* lse, void* workspace, size_t ws_bytes, ra_stream_t stream) {
+  const Range range("ra_decode_forward");
   ra_status st = check_decode(shp, c, layout);
   if (st != RA_OK) return st;
   if (out_dtype != RA_BF16 && out_dtype != RA_F32) return RA_ERR_INVALID;
@@ -552,6 +574,7 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
                                  int c, int layout, int causal, int overlap, int out_dtype,
                                  void* out, float* lse, void* workspace, size_t ws_bytes,
                                  ra_stream_t stream, ra_stream_t copy_stream) {
+  const Range range("ra_ring_forward_rotate");
   ra_status st = check_ring(shp, c, layout);
   if (st != RA_OK) return st;
   if (!out_dtype_ok(shp, out_dtype)) return RA_ERR_INVALID;
@@ -606,6 +629,7 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
     if (ce == cudaSuccess) ce = cudaStreamWaitEvent(xs, ev_prep, 0);
   }
   for (int t = 0; t < c && ce == cudaSuccess && st == RA_OK; ++t) {
+    const Range step(step_name(t));
     if (t > 0 && overlap) ce = cudaStreamWaitEvent(cs, ev_copy, 0);   // block for step t arrived
     if (ce != cudaSuccess) break;
     p.k = kbuf[t & 1];
