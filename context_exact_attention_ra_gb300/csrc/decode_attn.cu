@@ -173,9 +173,26 @@ __global__ void __launch_bounds__(kDecThreads)
   const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(p.v);
 
   // Stage the K and V rows of (piece pp, sub-chunk sc) into slot st.
+  // Natural position of shard-local key i0 + r for r in [0, 16): affine in r
+  // unless the 16 keys straddle the two chunks of a zig-zag shard.
+  const int half_n = p.n / 2;
+  auto chunk_base = [&](int shard, int i0, long long& nat0, int& step, bool& affine) {
+    affine = p.layout != RA_ZIGZAG || ((i0 < half_n) == (i0 + kSub - 1 < half_n));
+    step = p.layout == RA_STRIPED ? p.c : 1;
+    nat0 = natural_key(shard, i0, p.n, p.c, p.layout);
+  };
+  const long long row_elems = static_cast<long long>(p.Hkv) * D;     // between key rows
+  const __nv_bfloat16* kbg = kg + (static_cast<long long>(b) * p.S * p.Hkv + g) * D;
+  const __nv_bfloat16* vbg = vg + (static_cast<long long>(b) * p.S * p.Hkv + g) * D;
   auto issue = [&](int pp, int sc, int st) {
     const int shard = pp / p.pieces_per_shard;
     const int i0 = (pp % p.pieces_per_shard) * kPiece + sc * kSub;
+    const int iend = min(p.n, (pp % p.pieces_per_shard + 1) * kPiece);
+    long long nat0;
+    int step;
+    bool affine;
+    chunk_base(shard, i0, nat0, step, affine);
+    const long long nat_safe = natural_key(shard, 0, p.n, p.c, p.layout);   // rows past the end read nothing
     __nv_bfloat16* ks_ = wbase + st * L::kStage;
     __nv_bfloat16* vs_ = ks_ + kSub * L::kRow;
 #pragma unroll
@@ -183,11 +200,13 @@ __global__ void __launch_bounds__(kDecThreads)
       const int c = lane + 32 * u;
       const int rr = c / CH, cc = c % CH;
       const int i = i0 + rr;
-      const bool ok = i < p.n && i < (pp % p.pieces_per_shard + 1) * kPiece;
-      const long long nat = natural_key(shard, ok ? i : 0, p.n, p.c, p.layout);
-      const long long off = ((static_cast<long long>(b) * p.S + nat) * p.Hkv + g) * D + cc * 8;
-      cp_async16(smem_u32(ks_ + rr * L::kRow + cc * 8), kg + off, ok ? 16u : 0u);
-      cp_async16(smem_u32(vs_ + rr * L::kRow + cc * 8), vg + off, ok ? 16u : 0u);
+      const bool ok = i < iend;
+      long long nat = nat0 + static_cast<long long>(rr) * step;
+      if (!affine) nat = natural_key(shard, i, p.n, p.c, p.layout);
+      if (!ok) nat = nat_safe;
+      const long long off = nat * row_elems + cc * 8;
+      cp_async16(smem_u32(ks_ + rr * L::kRow + cc * 8), kbg + off, ok ? 16u : 0u);
+      cp_async16(smem_u32(vs_ + rr * L::kRow + cc * 8), vbg + off, ok ? 16u : 0u);
     }
     cp_async_commit();
   };
@@ -244,13 +263,19 @@ __global__ void __launch_bounds__(kDecThreads)
     }
     // ---- mask, running max, probabilities; this lane's four keys
     bool kvis[2][2][2];   // [n-tile][key of the pair][row half]
+    long long nat0;
+    int step;
+    bool affine;
+    chunk_base(shard, i0, nat0, step, affine);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
-        const int i = i0 + nt * 8 + 2 * tig + kk;
+        const int r = nt * 8 + 2 * tig + kk;
+        const int i = i0 + r;
         const bool in = i < pend;
-        const long long pos = (in && p.causal) ? natural_key(shard, i, p.n, p.c, p.layout) : 0;
+        const long long pos = affine ? nat0 + static_cast<long long>(r) * step
+                                     : natural_key(shard, i, p.n, p.c, p.layout);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) kvis[nt][kk][hf] = in && rvalid[hf] && (!p.causal || pos <= qpos[hf]);
       }
