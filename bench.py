@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--overlap-study", action="store_true",
                     help="time the ring with real K/V rotation, overlapped and not")
+    ap.add_argument("--lse-merge", type=int, default=0, metavar="P",
+                    help="time ra_lse_merge of P partial states of the workload's shape instead")
     ap.add_argument("--decode", action="store_true",
                     help="time decode over the sharded keys (one new token per step) instead")
     return ap.parse_args()
@@ -449,9 +451,62 @@ def run_overlap_study(args, rank, world, local):
         "flop": w.flops()}), flush=True)
 
 
+def run_lse_merge(args, rank, world, local):
+    """ra_lse_merge of P partial states (o fp32 [B,S,Hq,D], m, l [B,Hq,S]) of
+    the workload's shape into bf16 out + lse.  HBM-bound: the algorithmic bytes
+    are P*(4D + 8) per row read and 2D + 4 per row written."""
+    import torch
+
+    import context_exact_attention_ra_gb300 as ra
+    from workloads import WORKLOADS
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    P = args.lse_merge
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    outs = [torch.randn((w.B, w.S, w.Hq, w.D), generator=g, device=dev) for _ in range(P)]
+    ms = [torch.randn((w.B, w.Hq, w.S), generator=g, device=dev) * 4 for _ in range(P)]
+    ls = [torch.rand((w.B, w.Hq, w.S), generator=g, device=dev) * 100 + 1 for _ in range(P)]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ra.lse_merge(outs, ms, ls, torch.bfloat16)
+    ra.device_error()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ra.lse_merge(outs, ms, ls, torch.bfloat16)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ra.device_error()
+    ms_step = statistics.median(times)
+    rows = w.B * w.Hq * w.S
+    nbytes = rows * (P * (4 * w.D + 8) + 2 * w.D + 4)
+    peaks, kind = load_peaks()
+    gbs = nbytes / (ms_step * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "ra_lse_merge of P partial states: achieved GB/s", "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "dtype": "f32 in, bf16 out", "data": "synthetic",
+        "config": {"workload": f"{w.name} shape B={w.B} S={w.S} Hq={w.Hq} D={w.D}, P={P} partials",
+                   "l2": "flushed before every step"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                     "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                     "kernel": "merge_kernel" if P > 1 else "finalize_kernel"},
+        "gpu_launches": args.steps}), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.lse_merge > 0:
+        run_lse_merge(args, rank, world, local)
+        return
     if args.overlap_study:
         run_overlap_study(args, rank, world, local)
         return

@@ -175,23 +175,29 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams mp) {
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[r][i] = 0.f;
   }
-  for (int pi = 0; pi < mp.a.P; ++pi) {
+  // The loads of partial pi + 1 are issued before partial pi is folded in.
+  float mv[kMergeRows], lv[kMergeRows], ov[kMergeRows][V];
+  auto load = [&](int pi, float (&m_)[kMergeRows], float (&l_)[kMergeRows], float (&o_)[kMergeRows][V]) {
     const float* mpp = mp.a.ms[pi];
     const float* lpp = mp.a.ls[pi];
     const float* opp = mp.a.outs[pi];
-    float mv[kMergeRows], lv[kMergeRows], ov[kMergeRows][V];
 #pragma unroll
     for (int r = 0; r < kMergeRows; ++r) {
-      mv[r] = __ldg(mpp + si[r]);
-      lv[r] = __ldg(lpp + si[r]);
+      m_[r] = __ldg(mpp + si[r]);
+      l_[r] = __ldg(lpp + si[r]);
       if constexpr (V == 4) {
         const float4 f = __ldcs(reinterpret_cast<const float4*>(opp + oi[r]));
-        ov[r][0] = f.x; ov[r][1] = f.y; ov[r][2] = f.z; ov[r][3] = f.w;
+        o_[r][0] = f.x; o_[r][1] = f.y; o_[r][2] = f.z; o_[r][3] = f.w;
       } else {
         const float2 f = __ldcs(reinterpret_cast<const float2*>(opp + oi[r]));
-        ov[r][0] = f.x; ov[r][1] = f.y;
+        o_[r][0] = f.x; o_[r][1] = f.y;
       }
     }
+  };
+  load(0, mv, lv, ov);
+  for (int pi = 0; pi < mp.a.P; ++pi) {
+    float mn[kMergeRows], ln[kMergeRows], on[kMergeRows][V];
+    if (pi + 1 < mp.a.P) load(pi + 1, mn, ln, on);
 #pragma unroll
     for (int r = 0; r < kMergeRows; ++r) {
       if (mv[r] == -INFINITY) continue;   // an empty partial adds nothing
@@ -202,6 +208,15 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams mp) {
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[r][i] = fmaf(ov[r][i], w, acc[r][i] * alpha);
       M[r] = Mn;
+    }
+    if (pi + 1 < mp.a.P) {
+#pragma unroll
+      for (int r = 0; r < kMergeRows; ++r) {
+        mv[r] = mn[r];
+        lv[r] = ln[r];
+#pragma unroll
+        for (int i = 0; i < V; ++i) ov[r][i] = on[r][i];
+      }
     }
   }
 #pragma unroll
