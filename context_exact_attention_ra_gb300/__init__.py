@@ -311,18 +311,21 @@ def ring_forward_rotate(q, k, v, c, layout="zigzag", causal=True, overlap=True, 
 
 
 def decode_forward(q, q_pos, k, v, c, layout="zigzag", causal=True, scale=None, out_dtype=None,
-                   workspace=None, stream=None):
+                   workspace=None, stream=None, out=None, lse=None):
     """Attention of a few new tokens' queries q [B,R,Hq,D] (positions q_pos,
     int32 [R]) over k, v [B,S,Hkv,D] held in c shards: split-K partials per
-    shard piece, then their merge.  Returns (out [B,R,Hq,D], lse [B,Hq,R])."""
+    shard piece, then their merge.  Returns (out [B,R,Hq,D], lse [B,Hq,R]);
+    ``out``, ``lse`` and ``workspace`` may be given to reuse buffers."""
     _contig(q, k, v)
     lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     scale = q.shape[-1] ** -0.5 if scale is None else scale
     B, R, Hq, D = q.shape
     shp = Shape(B, R, k.shape[1], Hq, k.shape[2], D, _dtype_code(q), float(scale))
     ocode, odt = _out_code(out_dtype, q)
-    out = torch.empty((B, R, Hq, D), dtype=odt, device=q.device)
-    lse = torch.empty((B, Hq, R), dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty((B, R, Hq, D), dtype=odt, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, R), dtype=torch.float32, device=q.device)
     if workspace is None:
         need = int(lib().ra_decode_workspace_size(shp, int(c), lay))
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)

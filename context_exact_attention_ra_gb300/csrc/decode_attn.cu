@@ -40,7 +40,8 @@ constexpr int kSub = 16;         // keys per warp step: the MMA's K for P V
 constexpr int kPiece = 128;      // shard-local keys per piece
 constexpr int kTargetBlocks = 304;   // two resident blocks on each of 152 SMs
 constexpr int kStages = 3;           // staged 16-key chunks per warp (two loads in flight)
-constexpr int kMergeWarps = 8;
+constexpr int kMergeWarps = 32;
+constexpr int kMergeUnroll = 8;     // partial loads in flight per lane
 constexpr int kMergeThreads = kMergeWarps * 32;
 
 template <int D>
@@ -424,9 +425,9 @@ __global__ void __launch_bounds__(kDecThreads)
   }
 }
 
-// One block of 8 warps per (b, h, token) and 32-column slice of the head
+// One block of 32 warps per (b, h, token) and 32-column slice of the head
 // dimension: merge the P partials, normalise, write out (and, from the first
-// slice, lse).  Lane = column; the warps take every 8th partial with sixteen
+// slice, lse).  Lane = column; the warps take every 32nd partial with eight
 // loads in flight, and their sums are added in warp order.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
@@ -457,17 +458,17 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const float Mu = (M == -INFINITY) ? 0.f : M;
   float L = 0.f, acc = 0.f;
   int i = warp;
-  for (; i + 15 * kMergeWarps < p.P; i += 16 * kMergeWarps) {
-    float m[16], l[16], o[16];
+  for (; i + (kMergeUnroll - 1) * kMergeWarps < p.P; i += kMergeUnroll * kMergeWarps) {
+    float m[kMergeUnroll], l[kMergeUnroll], o[kMergeUnroll];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
+    for (int u = 0; u < kMergeUnroll; ++u) {
       const long long ii = i + u * kMergeWarps;
       m[u] = pm[ii * mstride];
       l[u] = pl[ii * mstride];
       o[u] = po[ii * ostride];
     }
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
+    for (int u = 0; u < kMergeUnroll; ++u) {
       const float f = (m[u] == -INFINITY) ? 0.f : exp2f(m[u] - Mu);
       L = fmaf(l[u], f, L);
       acc = fmaf(o[u], f, acc);
