@@ -22,13 +22,13 @@
 //   warps 4-7  softmax for Q1
 //   warp 8     TMA loads of Q and the K tiles
 //   warp 9     TMA loads of the V tiles
-//   warp 10    tensor-memory allocation and tcgen05.mma issue
+//   warp 10    tensor-memory allocation; its lane 0 alone issues tcgen05.mma
 // Pipelines: K and V each have 2 shared-memory stages; the two query tiles
 // ping-pong so that the tensor core multiplies one tile while the softmax of
 // the other runs.  Tensor memory (512 columns): S0 | S1 | O0 | O1, with P_h
 // stored as packed bf16 over the first 64 columns of S_h.
 //
-// Every mbarrier wait is bounded (4 s); a wait that runs out raises an abort
+// Every mbarrier wait is bounded (ra_wait.cuh, 4 s); a wait that runs out raises an abort
 // flag in shared memory and a bit in the device error word, every role
 // leaves its loop, outstanding tensor-core work and TMA loads are drained
 // (bounded), tensor memory is freed and the block exits.

@@ -192,20 +192,6 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// ---- register reallocation between warpgroups ------------------------------
-
-// Give registers back to the block's pool / take them from it; executed by
-// all four warps of a warpgroup.  Counts are multiples of 8 in [24, 256].
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ---- arithmetic ------------------------------------------------------------
 
 __device__ __forceinline__ float ex2(float x) {
