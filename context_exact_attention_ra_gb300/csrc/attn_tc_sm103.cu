@@ -40,7 +40,6 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
 #include "ra_internal.h"
 #include "ra_wait.cuh"
@@ -710,46 +709,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launch.
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn(int* err) {
-  static EncodeTiledFn fn = nullptr;
-  static int status = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                                     cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || f == nullptr)
-      status = (e != cudaSuccess) ? static_cast<int>(e) : static_cast<int>(cudaErrorNotSupported);
-    else
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  *err = status;
-  return fn;
-}
-
-// [B][rows][H][D] bf16 tensor, boxes of 64 columns x 1 head x 128 rows.
-int make_map(CUtensorMap* map, const void* base, int B, long long rows, int H, int D) {
-  int err = 0;
-  EncodeTiledFn fn = encode_fn(&err);
-  if (fn == nullptr) return err ? err : static_cast<int>(cudaErrorNotSupported);
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
-                           static_cast<cuuint64_t>(rows) * H * D * 2};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTile), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? 0 : static_cast<int>(cudaErrorInvalidValue);
-}
-
 template <int D>
 int launch_d(const AttnParams& p, const void* q, const void* k, const void* v,
              long long q_rows_total, long long k_rows_total, cudaStream_t stream) {
@@ -758,9 +717,9 @@ int launch_d(const AttnParams& p, const void* q, const void* k, const void* v,
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
   launch_stage() = "cuTensorMapEncodeTiled";
-  int e = make_map(&mq, q, p.B, q_rows_total, p.Hq, D);
-  if (!e) e = make_map(&mk, k, p.B, k_rows_total, p.Hkv, D);
-  if (!e) e = make_map(&mv, v, p.B, k_rows_total, p.Hkv, D);
+  int e = make_tma_map_bf16(&mq, q, p.B, q_rows_total, p.Hq, D, kTile);
+  if (!e) e = make_tma_map_bf16(&mk, k, p.B, k_rows_total, p.Hkv, D, kTile);
+  if (!e) e = make_tma_map_bf16(&mv, v, p.B, k_rows_total, p.Hkv, D, kTile);
   if (e) return e;
   const int smem = Smem<D>::kDynamic;
   launch_stage() = "cudaFuncSetAttribute (tensor-core kernel)";

@@ -533,11 +533,16 @@ int launch_partial(const DecodeParams& p, dim3 grid, cudaStream_t s) {
 
 int launch_decode(const DecodeParams& p, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int G = p.Hq / p.Hkv;
-  const int row_blocks = (G * p.R + kDecRows - 1) / kDecRows;
-  dim3 grid(static_cast<unsigned>(p.B * p.Hkv * row_blocks), static_cast<unsigned>(p.P));
-  launch_stage() = "decode partial kernel launch";
-  int e = (p.D == 128) ? launch_partial<128>(p, grid, s) : launch_partial<64>(p, grid, s);
+  int e = 0;
+  if (decode_tc_applies(p.D, p.n, p.layout)) {
+    e = launch_decode_tc(p, stream);
+  } else {
+    const int G = p.Hq / p.Hkv;
+    const int row_blocks = (G * p.R + kDecRows - 1) / kDecRows;
+    dim3 grid(static_cast<unsigned>(p.B * p.Hkv * row_blocks), static_cast<unsigned>(p.P));
+    launch_stage() = "decode partial kernel launch";
+    e = (p.D == 128) ? launch_partial<128>(p, grid, s) : launch_partial<64>(p, grid, s);
+  }
   if (e != 0) return e;
   const dim3 mgrid(static_cast<unsigned>(static_cast<long long>(p.B) * p.Hq * p.R),
                    static_cast<unsigned>(p.D / 32));

@@ -1,0 +1,508 @@
+// Decode over keys and values spread across c shards on the sm_103a tensor
+// cores: split-K partial states per block, merged afterwards
+// ("06 - Sequence / Context Parallelism", section 7: attention of a new query
+// over distributed keys is a gather of partial results, like a split-K).
+//
+// A block owns the (at most 16) query rows of one (batch, key/value head) --
+// the G heads sharing the head times the new tokens -- and a fixed set of
+// 128-key tiles (tile pi, pi + P, ... over all shards' tiles), and writes one
+// partial online-softmax state (o, m, l) for them.  The 16 query rows are too
+// few for the M of tcgen05.mma, so the products are taken transposed, with the
+// 128 keys (or the 128 output columns) as M and the 16 query rows as N:
+//   S^T = K Q^T        A = K tile (K-major), B = Q (K-major)      -> TMEM, lane = key
+//   O^T += V^T P^T     A = V tile read M-major, B = P^T (K-major) -> TMEM, lane = column
+// Each softmax thread owns one key of the tile (one TMEM lane): it scales and
+// masks its 16 scores, the block's maximum per query row is reduced across the
+// 128 threads (shuffles, then four warps through shared memory), it writes its
+// 16 probabilities into the P^T operand as a bf16 head plus a bf16 remainder
+// (so P enters the product with about 16 bits, and the result stays within
+// 1e-4 of the float64 definition) and keeps its own share of the row sums; every thread also owns one output column of O^T and rescales it
+// when a row's maximum rose.  K and V tiles stream through three shared-memory
+// stages by TMA, so the block reads each key and value byte once, and the
+// kernel is bound by HBM bandwidth.
+//
+// Warp roles (192 threads): warps 0-3 softmax and epilogue, warp 4 TMA loads,
+// warp 5 tensor-memory allocation; its lane 0 issues the MMAs.  Every wait is
+// bounded (ra_wait.cuh).
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include "ra_internal.h"
+#include "ra_wait.cuh"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kDTRows = 16;           // query rows per block: the MMAs' N
+constexpr int kDTKeys = 128;          // keys per tile
+constexpr int kDTD = 128;             // head dimension of this kernel
+constexpr int kDTStages = 3;
+constexpr int kDTWarpLoad = 4;
+constexpr int kDTWarpMma = 5;
+constexpr int kDTThreads = 6 * 32;
+constexpr uint32_t kDTTmemCols = 64;  // S0 | S1 | O, 16 columns each
+constexpr int kDTTargetBlocks = 152;  // one resident block per SM
+
+struct DTSmem {
+  static constexpr int kBox = 64;                            // bf16 columns per 128-byte row
+  static constexpr int kKVBox = kDTKeys * kBox * 2;          // 16 KB: 128 keys x 64 columns
+  static constexpr int kKVTile = 2 * kKVBox;                 // 32 KB: 128 keys x 128 columns
+  static constexpr int kRowsBox = kDTRows * kBox * 2;        // 2 KB: 16 rows x 64 columns
+  static constexpr int kQ = 0;                               // Q: 16 rows x 128 columns (2 boxes)
+  static constexpr int kPBuf = 2 * 2 * kRowsBox;             // P^T head and remainder, 16 x 128 each
+  static constexpr int kP = kQ + 2 * kRowsBox;               // two such buffers
+  static constexpr int kK = kP + 2 * kPBuf;
+  static constexpr int kV = kK + kDTStages * kKVTile;
+  static constexpr int kBar = kV + kDTStages * kKVTile;
+  static constexpr int bKVFull = 0;
+  static constexpr int bKVEmpty = bKVFull + kDTStages;
+  static constexpr int bSFull = bKVEmpty + kDTStages;
+  static constexpr int bPFull = bSFull + 2;
+  static constexpr int bPVDone = bPFull + 2;
+  static constexpr int bXch = bPVDone + 1;                   // row-max exchange, 2 parities
+  static constexpr int bDrain = bXch + 2;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;          // tmem slot, abort flag
+  static constexpr int kRed = kMisc + 16;                    // [2][4 warps][16] floats
+  static constexpr int kBytes = kRed + 2 * 4 * kDTRows * 4;
+  static constexpr int kDynamic = kBytes + 1024;
+  static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kP % 1024 == 0, "swizzle atoms are 1024 bytes");
+  static_assert(kDynamic <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ long long dt_natural_key(int r, int i, int n, int c, int layout) {
+  if (layout == RA_ZIGZAG) {
+    const int ch = n / 2;
+    return i < ch ? static_cast<long long>(r) * ch + i : static_cast<long long>(2 * c - 1 - r) * ch + (i - ch);
+  }
+  if (layout == RA_STRIPED) return r + static_cast<long long>(c) * i;
+  return static_cast<long long>(r) * n + i;
+}
+
+// Byte offset of element (row, col) of a K-major operand with 128-byte rows
+// and the 128-byte swizzle (16-byte chunk c of row r sits at chunk c ^ (r % 8)),
+// boxes of box_bytes per 64 columns.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int box_bytes) {
+  const int box = col >> 6;
+  const int k = col & 63;
+  return static_cast<uint32_t>(box * box_bytes + row * 128 + (((k >> 3) ^ (row & 7)) << 4) + ((k & 7) << 1));
+}
+
+// Maximum (or sum) of 16 per-thread values over the 32 lanes of a warp with
+// 16 shuffles: after the call, lane L holds the result for row
+// ((L>>4)&1)*8 + ((L>>3)&1)*4 + ((L>>2)&1)*2 + ((L>>1)&1) (lanes L and L^1 agree).
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
+  float a8[8], a4[4], a2[2];
+  const bool h1 = (lane >> 4) & 1, h2 = (lane >> 3) & 1, h3 = (lane >> 2) & 1, h4 = (lane >> 1) & 1;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float mine = h1 ? v[8 + k] : v[k];
+    const float other = h1 ? v[k] : v[8 + k];
+    const float r = __shfl_xor_sync(0xffffffffu, other, 16);
+    a8[k] = kMax ? fmaxf(mine, r) : mine + r;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float mine = h2 ? a8[4 + k] : a8[k];
+    const float other = h2 ? a8[k] : a8[4 + k];
+    const float r = __shfl_xor_sync(0xffffffffu, other, 8);
+    a4[k] = kMax ? fmaxf(mine, r) : mine + r;
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float mine = h3 ? a4[2 + k] : a4[k];
+    const float other = h3 ? a4[k] : a4[2 + k];
+    const float r = __shfl_xor_sync(0xffffffffu, other, 4);
+    a2[k] = kMax ? fmaxf(mine, r) : mine + r;
+  }
+  const float mine = h4 ? a2[1] : a2[0];
+  const float other = h4 ? a2[0] : a2[1];
+  const float r = __shfl_xor_sync(0xffffffffu, other, 2);
+  float a = kMax ? fmaxf(mine, r) : mine + r;
+  const float r1 = __shfl_xor_sync(0xffffffffu, a, 1);
+  return kMax ? fmaxf(a, r1) : a + r1;
+}
+
+__device__ __forceinline__ int reduced_row(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
+__global__ void __launch_bounds__(kDTThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const DecodeParams p) {
+  using L = DTSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const Abort ab{abort_flag, p.err};
+  float* const red = reinterpret_cast<float*>(smem + L::kRed);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.Hq / p.Hkv;
+  const int rows = G * p.R;
+  const int row_blocks = (rows + kDTRows - 1) / kDTRows;
+  const int bx = blockIdx.x;
+  const int rb = bx % row_blocks;
+  const int g = (bx / row_blocks) % p.Hkv;
+  const int b = bx / (row_blocks * p.Hkv);
+  const int pi = blockIdx.y;
+  const int row0 = rb * kDTRows;
+  const int nrows = min(kDTRows, rows - row0);
+  const int tps = (p.n + kDTKeys - 1) / kDTKeys;   // tiles per shard
+  const int T = p.c * tps;
+  const int J = (pi < T) ? (T - 1 - pi) / p.P + 1 : 0;   // tiles of this block
+  auto tile_of = [&](int j, int& shard, int& lt) {
+    const int ti = pi + j * p.P;
+    shard = ti / tps;
+    lt = ti % tps;
+  };
+
+  // ---- set-up --------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDTStages; ++s) {
+      ptx::mbar_init(bar(L::bKVFull + s), 1);
+      ptx::mbar_init(bar(L::bKVEmpty + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(L::bSFull + i), 1);
+      ptx::mbar_init(bar(L::bPFull + i), 128);
+      ptx::mbar_init(bar(L::bXch + i), 128);
+    }
+    ptx::mbar_init(bar(L::bPVDone), 1);
+    ptx::mbar_init(bar(L::bDrain), 1);
+    *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.err) != 0) ? 1 : 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kDTWarpLoad && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_k);
+    ptx::tma_prefetch_desc(&tm_v);
+  }
+  if (warp == kDTWarpMma) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kDTTmemCols);
+    ptx::tmem_relinquish();
+  }
+  // Q: 16 rows x 128 columns, K-major with the 128-byte swizzle; row
+  // n = (head within group) * R + token, rows past the block's rows are zero.
+  int qpos[kDTRows];
+  bool rvalid[kDTRows];
+#pragma unroll
+  for (int n = 0; n < kDTRows; ++n) {
+    rvalid[n] = n < nrows;
+    qpos[n] = rvalid[n] ? p.q_pos[(row0 + n) % p.R] : INT_MIN;
+  }
+  if (warp < 4) {
+    const int t = threadIdx.x;
+    const int n = t >> 3;              // row
+    const int d0 = (t & 7) * 16;       // 16 columns
+    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = make_uint4(0, 0, 0, 0);
+    if (n < nrows) {
+      const int rr = row0 + n;
+      const int h = g * G + rr / p.R;
+      const int tok = rr % p.R;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                        ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * kDTD + d0);
+      w0 = src[0];
+      w1 = src[1];
+    }
+    *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(n, d0, L::kRowsBox)) = w0;
+    *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(n, d0 + 8, L::kRowsBox)) = w1;
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kDTWarpLoad) {
+    // ===================== TMA loads of the K and V tiles =================
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = !*abort_flag;
+      for (int j = 0; j < J && ok; ++j) {
+        const int st = j % kDTStages;
+        if (j >= kDTStages) ok = wait_bar(bar(L::bKVEmpty + st), ((j / kDTStages) - 1) & 1u, ab, kErrTimeoutEmpty);
+        if (!ok) break;
+        int shard, lt;
+        tile_of(j, shard, lt);
+        const int nat0 = static_cast<int>(dt_natural_key(shard, lt * kDTKeys, p.n, p.c, p.layout));
+        ptx::mbar_arrive_expect_tx(bar(L::bKVFull + st), 2 * L::kKVTile);
+        for (int x = 0; x < 2; ++x) {
+          ptx::tma_load_4d(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
+                           x * L::kBox, g, nat0, b);
+          ptx::tma_load_4d(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
+                           x * L::kBox, g, nat0, b);
+        }
+        ++issued;
+      }
+      if (*abort_flag) {
+        // let the loads still in flight land before the block exits
+        for (int s = 0; s < kDTStages; ++s) {
+          const int cnt = (issued > s) ? (issued - 1 - s) / kDTStages + 1 : 0;
+          if (cnt > 0) wait_bar_drain(bar(L::bKVFull + s), (cnt - 1) & 1u);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kDTWarpMma) {
+    // ===================== tensor-core issue ============================
+    if (lane == 0) {
+      constexpr uint32_t idS = ptx::idesc_bf16_f32(128, kDTRows, false, false);
+      constexpr uint32_t idPV = ptx::idesc_bf16_f32(128, kDTRows, false, true);
+      const uint64_t dQ = ptx::smem_desc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t dK = ptx::smem_desc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t dV = ptx::smem_desc_sw128(sbase + L::kV, L::kKVBox, 1024);
+      const uint64_t dP = ptx::smem_desc_sw128(sbase + L::kP, 16, 1024);
+      bool ok = true;
+      bool issued_any = false;
+      auto issue_S = [&](int st, int sb) {
+        const uint64_t kd = dK + static_cast<uint64_t>((st * L::kKVTile) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kDTD / 16; ++kk) {
+          const uint64_t oa = static_cast<uint64_t>(((kk / 4) * L::kKVBox + (kk % 4) * 32) >> 4);
+          const uint64_t ob = static_cast<uint64_t>(((kk / 4) * L::kRowsBox + (kk % 4) * 32) >> 4);
+          ptx::tc_mma_ss(tmem + sb * kDTRows, kd + oa, dQ + ob, idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_PV = [&](int st, int pb) {
+        const uint64_t vd = dV + static_cast<uint64_t>((st * L::kKVTile) >> 4);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {   // bf16 head of P, then its remainder
+          const uint64_t pd = dP + static_cast<uint64_t>((pb * L::kPBuf + part * 2 * L::kRowsBox) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kDTKeys / 16; ++kk) {
+            const uint64_t oa = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+            const uint64_t ob = static_cast<uint64_t>(((kk / 4) * L::kRowsBox + (kk % 4) * 32) >> 4);
+            ptx::tc_mma_ss(tmem + 2 * kDTRows, vd + oa, pd + ob, idPV, 1u);
+          }
+        }
+      };
+      for (int j = 0; j < J && ok; ++j) {
+        const int st = j % kDTStages;
+        ok = wait_bar(bar(L::bKVFull + st), (j / kDTStages) & 1u, ab, kErrTimeoutK);
+        if (!ok) break;
+        ptx::tc_fence_after_sync();
+        issue_S(st, j & 1);
+        ptx::tc_commit(bar(L::bSFull + (j & 1)));
+        issued_any = true;
+        if (j >= 1) {
+          ok = wait_bar(bar(L::bPFull + ((j - 1) & 1)), ((j - 1) >> 1) & 1u, ab, kErrTimeoutP);
+          if (!ok) break;
+          ptx::tc_fence_after_sync();
+          issue_PV((j - 1) % kDTStages, (j - 1) & 1);
+          ptx::tc_commit(bar(L::bPVDone));
+          ptx::tc_commit(bar(L::bKVEmpty + (j - 1) % kDTStages));
+        }
+      }
+      if (ok && J > 0) {
+        ok = wait_bar(bar(L::bPFull + ((J - 1) & 1)), ((J - 1) >> 1) & 1u, ab, kErrTimeoutP);
+        if (ok) {
+          ptx::tc_fence_after_sync();
+          issue_PV((J - 1) % kDTStages, (J - 1) & 1);
+          ptx::tc_commit(bar(L::bPVDone));
+        }
+      }
+      if (!ok && issued_any) {
+        ptx::tc_commit(bar(L::bDrain));
+        if (!wait_bar_drain(bar(L::bDrain), 0)) atomicOr(p.err, kErrTimeoutDrain);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ===================== softmax: thread t owns key t of each tile ========
+    const int t = threadIdx.x;                        // also the output column of O^T
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_base + 2 * kDTRows;
+    {
+      uint32_t z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0u;
+      ptx::tmem_st16(tO, z);
+      ptx::tmem_wait_st();
+    }
+    float m_run[kDTRows], lpart[kDTRows];
+#pragma unroll
+    for (int n = 0; n < kDTRows; ++n) {
+      m_run[n] = -INFINITY;
+      lpart[n] = 0.f;
+    }
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < J && ok; ++j) {
+      const int sb = j & 1;
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bSFull + sb), (j >> 1) & 1u, ab, kErrTimeoutS));
+      if (!ok) break;
+      ptx::tc_fence_after_sync();
+      uint32_t su[16];
+      ptx::tmem_ld16(tmem + lane_base + sb * kDTRows, su);
+      int shard, lt;
+      tile_of(j, shard, lt);
+      const int i = lt * kDTKeys + t;
+      const bool kvalid = i < p.n;
+      const long long pos = dt_natural_key(shard, kvalid ? i : 0, p.n, p.c, p.layout);
+      float x[kDTRows];
+#pragma unroll
+      for (int n = 0; n < kDTRows; ++n) {
+        const bool vis = kvalid && rvalid[n] && (!p.causal || pos <= qpos[n]);
+        x[n] = vis ? __uint_as_float(su[n]) * sl2 : -INFINITY;
+      }
+      // block maximum per query row: 16 shuffles per warp, then the 4 warps
+      const float wm = warp_reduce16<true>(x, lane);
+      float* rbuf = red + sb * 4 * kDTRows;
+      if ((lane & 1) == 0) rbuf[warp * kDTRows + reduced_row(lane)] = wm;
+      ptx::mbar_arrive(bar(L::bXch + sb));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bXch + sb), (j >> 1) & 1u, ab, kErrTimeoutS));
+      if (!ok) break;
+      float alpha[kDTRows], muse[kDTRows];
+      bool any_rescale = false;
+#pragma unroll
+      for (int n = 0; n < kDTRows; ++n) {
+        const float tmax = fmaxf(fmaxf(rbuf[n], rbuf[kDTRows + n]), fmaxf(rbuf[2 * kDTRows + n], rbuf[3 * kDTRows + n]));
+        const float m_new = fmaxf(m_run[n], tmax);
+        muse[n] = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[n] = (m_run[n] == m_new) ? 1.f : ptx::ex2(m_run[n] - m_new);
+        any_rescale |= (alpha[n] != 1.f) && (m_run[n] != -INFINITY);
+        m_run[n] = m_new;
+      }
+      // probabilities: this thread's column of P^T (bf16) and its share of l
+      uint8_t* pbuf = smem + L::kP + sb * L::kPBuf;
+#pragma unroll
+      for (int n = 0; n < kDTRows; ++n) {
+        const float pr = (x[n] == -INFINITY) ? 0.f : ptx::ex2(x[n] - muse[n]);
+        lpart[n] = lpart[n] * alpha[n] + pr;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(pr);
+        const uint32_t off = sw128_offset(n, t, L::kRowsBox);
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + 2 * L::kRowsBox + off) =
+            __float2bfloat16_rn(pr - __bfloat162float(hi));
+      }
+      // rescale this thread's column of O^T once the previous P V has run
+      if (j >= 1) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone), (j - 1) & 1u, ab, kErrTimeoutO));
+        if (!ok) break;
+        ptx::tc_fence_after_sync();
+        if (any_rescale) {
+          uint32_t u[16];
+          ptx::tmem_ld16(tO, u);
+#pragma unroll
+          for (int n = 0; n < kDTRows; ++n) u[n] = __float_as_uint(__uint_as_float(u[n]) * alpha[n]);
+          ptx::tmem_st16(tO, u);
+          ptx::tmem_wait_st();
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before_sync();
+      ptx::mbar_arrive(bar(L::bPFull + sb));
+    }
+
+    // ---- epilogue: the block's partial state ------------------------------
+    if (ok && J > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone), (J - 1) & 1u, ab, kErrTimeoutO));
+      if (ok) ptx::tc_fence_after_sync();
+    }
+    if (ok) {
+      // row sums over the 128 threads, reusing the exchange buffers in warp order
+      const float ws = warp_reduce16<false>(lpart, lane);
+      float* rbuf = red + (J & 1) * 4 * kDTRows;
+      if ((lane & 1) == 0) rbuf[warp * kDTRows + reduced_row(lane)] = ws;
+      ptx::mbar_arrive(bar(L::bXch + (J & 1)));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bXch + (J & 1)), (J >> 1) & 1u, ab, kErrTimeoutS));
+      if (ok) {
+        uint32_t u[16];
+        ptx::tmem_ld16(tO, u);
+#pragma unroll
+        for (int n = 0; n < kDTRows; ++n) {
+          if (n >= nrows) break;
+          const int rr = row0 + n;
+          const int h = g * G + rr / p.R;
+          const int tok = rr % p.R;
+          // partial layout: o [P, B, R, Hq, D]; m, l [P, B, Hq, R]
+          p.part_o[(((static_cast<long long>(pi) * p.B + b) * p.R + tok) * p.Hq + h) * kDTD + t] =
+              __uint_as_float(u[n]);
+        }
+        if (t < nrows) {
+          const int n = t;
+          float lsum = 0.f;
+          float mr = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) lsum += rbuf[w * kDTRows + n];
+#pragma unroll
+          for (int k = 0; k < kDTRows; ++k)
+            if (k == n) mr = m_run[k];
+          const int rr = row0 + n;
+          const int h = g * G + rr / p.R;
+          const int tok = rr % p.R;
+          const long long pm = ((static_cast<long long>(pi) * p.B + b) * p.Hq + h) * p.R + tok;
+          p.part_m[pm] = mr;
+          p.part_l[pm] = lsum;
+        }
+      }
+    }
+  }
+
+  // ---- teardown -------------------------------------------------------------
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kDTWarpMma) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem, kDTTmemCols);
+  }
+}
+
+}  // namespace
+
+bool decode_tc_applies(int D, int n, int layout) {
+  if (D != kDTD || n <= 0) return false;
+  if (layout == RA_CONTIGUOUS) return true;
+  return layout == RA_ZIGZAG && (n / 2) % kDTKeys == 0;
+}
+
+int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c) {
+  const long long tiles = static_cast<long long>(c) * ((n + kDTKeys - 1) / kDTKeys);
+  const long long units = static_cast<long long>(B) * Hkv * ((static_cast<long long>(G) * R + kDTRows - 1) / kDTRows);
+  long long want = (kDTTargetBlocks + units - 1) / units;
+  if (want < 1) want = 1;
+  if (want > tiles) want = tiles;
+  const long long per = (tiles + want - 1) / want;
+  return static_cast<int>((tiles + per - 1) / per);
+}
+
+int launch_decode_tc(const DecodeParams& p, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap mk, mv;
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  launch_stage() = "cuTensorMapEncodeTiled (decode)";
+  int e = make_tma_map_bf16(&mk, p.k, p.B, p.S, p.Hkv, kDTD, kDTKeys);
+  if (!e) e = make_tma_map_bf16(&mv, p.v, p.B, p.S, p.Hkv, kDTD, kDTKeys);
+  if (e) return e;
+  static int done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+  if (!done[dev]) {
+    launch_stage() = "cudaFuncSetAttribute (decode tensor-core kernel)";
+    const cudaError_t ce = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                DTSmem::kDynamic);
+    if (ce != cudaSuccess) return static_cast<int>(ce);
+    done[dev] = 1;
+  }
+  const int G = p.Hq / p.Hkv;
+  const int row_blocks = (G * p.R + kDTRows - 1) / kDTRows;
+  dim3 grid(static_cast<unsigned>(p.B * p.Hkv * row_blocks), static_cast<unsigned>(p.P));
+  launch_stage() = "decode tensor-core kernel launch";
+  decode_tc_kernel<<<grid, kDTThreads, DTSmem::kDynamic, s>>>(mk, mv, p);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace ra

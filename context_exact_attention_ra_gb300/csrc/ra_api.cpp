@@ -492,10 +492,12 @@ struct DecodeWs {
   size_t o, m, l, total;
 };
 
-DecodeWs decode_ws(const ra_shape& s, int c) {
+DecodeWs decode_ws(const ra_shape& s, int c, int layout) {
   DecodeWs w;
   const int n = s.Sk / c;
-  w.P = ra::decode_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, c * ra::decode_pieces_per_shard(n));
+  w.P = ra::decode_tc_applies(s.D, n, layout)
+            ? ra::decode_tc_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, n, c)
+            : ra::decode_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, c * ra::decode_pieces_per_shard(n));
   const size_t P = static_cast<size_t>(w.P), B = static_cast<size_t>(s.B), R = static_cast<size_t>(s.Sq);
   size_t off = 0;
   w.o = off;  off = round_up(off + P * B * R * s.Hq * s.D * sizeof(float));
@@ -517,7 +519,7 @@ ra_status check_decode(const ra_shape& s, int c, int layout) {
 
 size_t ra_decode_workspace_size(ra_shape shp, int c, int layout) {
   if (check_decode(shp, c, layout) != RA_OK || shp.Sk == 0) return 0;
-  return decode_ws(shp, c).total;
+  return decode_ws(shp, c, layout).total;
 }
 
 ra_status ra_decode_forward(const void* q, const int32_t* q_pos, const void* k, const void* v,
@@ -530,7 +532,7 @@ ra_status ra_decode_forward(const void* q, const int32_t* q_pos, const void* k, 
   if (shp.B == 0 || shp.Sq == 0 || shp.Sk == 0) return RA_OK;
   if (!q || !q_pos || !k || !v || !out) return RA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_INVALID;
-  const DecodeWs w = decode_ws(shp, c);
+  const DecodeWs w = decode_ws(shp, c, layout);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       ws_bytes < w.total)
     return RA_ERR_WORKSPACE;
@@ -560,6 +562,9 @@ ra_status ra_decode_forward(const void* q, const int32_t* q_pos, const void* k, 
   p.out = out;
   p.out_f32 = out_dtype == RA_F32 ? 1 : 0;
   p.lse = lse;
+  int err = 0;
+  p.err = ra::device_error_word(&err);
+  if (p.err == nullptr) return cuda_fail(err, "device error word lookup");
   return cuda_status(ra::launch_decode(p, stream));
 }
 

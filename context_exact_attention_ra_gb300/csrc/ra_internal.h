@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <vector_types.h>
 
 #include "ra.h"
@@ -76,6 +77,7 @@ struct DecodeParams {
   void* out;                   // [B, R, Hq, D]
   int out_f32;
   float* lse;                  // [B, Hq, R] or nullptr
+  unsigned int* err;           // device error word (bounded waits that ran out)
 };
 
 // Error bits written into the device error word.
@@ -92,6 +94,10 @@ enum : unsigned int {
 };
 
 // ---- launchers (return a cudaError_t as int; 0 = success) -------------
+// Tensor map over a [B][rows][H][D] bf16 tensor: boxes of 64 columns x 1 head x
+// box_rows rows, 128-byte swizzle (ra_tma.cpp).  Returns a cudaError_t value.
+int make_tma_map_bf16(CUtensorMap* map, const void* base, int B, long long rows, int H, int D,
+                      int box_rows);
 int launch_attn_tc(const AttnParams& p, const void* q, const void* k, const void* v,
                    long long q_rows_total, long long k_rows_total, void* stream);
 int launch_attn_f32(const AttnParams& p, void* stream);
@@ -115,6 +121,12 @@ int launch_decode(const DecodeParams& p, void* stream);
 int decode_pieces_per_shard(int n);
 // Number of partial states (blocks per batch, key/value head and row block).
 int decode_partials(int B, int Hkv, int G, int R, int pieces);
+// The tensor-core decode (decode_tc_sm103.cu): D = 128 and 128-key tiles that
+// are contiguous in natural order (contiguous shards, or zig-zag chunks of a
+// multiple of 128 keys); otherwise the warp-level kernel runs.
+bool decode_tc_applies(int D, int n, int layout);
+int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c);
+int launch_decode_tc(const DecodeParams& p, void* stream);
 unsigned int* device_error_word(int* cuda_err);
 // Name of the host step that produced the last launcher error (thread-local).
 const char*& launch_stage();

@@ -1,0 +1,58 @@
+// Host side of the TMA loads: tensor maps over [B][rows][H][D] bf16 tensors.
+// The driver's cuTensorMapEncodeTiled is looked up once through the runtime.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(int* err) {
+  static EncodeTiledFn fn = nullptr;
+  static int status = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || f == nullptr)
+      status = (e != cudaSuccess) ? static_cast<int>(e) : static_cast<int>(cudaErrorNotSupported);
+    else
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  *err = status;
+  return fn;
+}
+
+}  // namespace
+
+// Boxes of 64 columns (128 bytes, 128-byte swizzle) x 1 head x box_rows rows;
+// rows past the end of the tensor read as zeros.
+int make_tma_map_bf16(CUtensorMap* map, const void* base, int B, long long rows, int H, int D,
+                      int box_rows) {
+  int err = 0;
+  EncodeTiledFn fn = encode_fn(&err);
+  if (fn == nullptr) return err ? err : static_cast<int>(cudaErrorNotSupported);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(rows) * H * D * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(cudaErrorInvalidValue);
+}
+
+}  // namespace ra
