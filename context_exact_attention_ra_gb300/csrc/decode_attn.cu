@@ -27,6 +27,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <cstring>
 
 #include "ra_internal.h"
 
@@ -41,7 +42,7 @@ constexpr int kPiece = 128;      // shard-local keys per piece
 constexpr int kTargetBlocks = 304;   // two resident blocks on each of 152 SMs
 constexpr int kStages = 3;           // staged 16-key chunks per warp (two loads in flight)
 constexpr int kMergeWarps = 32;
-constexpr int kMergeUnroll = 8;     // partial loads in flight per lane
+constexpr int kMergeUnroll = 5;     // partial loads in flight per lane
 constexpr int kMergeThreads = kMergeWarps * 32;
 
 template <int D>
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kDecThreads)
     }
   }
 
+  asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled early
   float o[DT][4];
 #pragma unroll
   for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -427,13 +429,16 @@ __global__ void __launch_bounds__(kDecThreads)
 
 // One block of 32 warps per (b, h, token) and 32-column slice of the head
 // dimension: merge the P partials, normalise, write out (and, from the first
-// slice, lse).  Lane = column; the warps take every 32nd partial with eight
-// loads in flight, and their sums are added in warp order.
+// slice, lse).  Lane = column; the warps take every 32nd partial (five loads
+// in flight) and fold them in one online pass; the warps' states are then
+// combined in warp order.  Launched as a dependent of the partial kernel: it
+// waits for that grid to finish before it reads the partials.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
-  __shared__ float red[kMergeWarps];
+  __shared__ float red_m[kMergeWarps];
   __shared__ float red_l[kMergeWarps];
   __shared__ float red_o[kMergeWarps][32];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long row = blockIdx.x;
@@ -446,59 +451,54 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const float* pm = p.part_m + (static_cast<long long>(b) * p.Hq + h) * p.R + tok;
   const float* pl = p.part_l + (static_cast<long long>(b) * p.Hq + h) * p.R + tok;
   const float* po = p.part_o + ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * D + col;
-  float M = -INFINITY;
-  for (int i = threadIdx.x; i < p.P; i += kMergeThreads) M = fmaxf(M, pm[i * mstride]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = red[0];
-#pragma unroll
-  for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
-  const float Mu = (M == -INFINITY) ? 0.f : M;
-  float L = 0.f, acc = 0.f;
-  int i = warp;
-  for (; i + (kMergeUnroll - 1) * kMergeWarps < p.P; i += kMergeUnroll * kMergeWarps) {
+  float M = -INFINITY, L = 0.f, acc = 0.f;
+  for (int i = warp; i < p.P; i += kMergeUnroll * kMergeWarps) {
     float m[kMergeUnroll], l[kMergeUnroll], o[kMergeUnroll];
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
       const long long ii = i + u * kMergeWarps;
-      m[u] = pm[ii * mstride];
-      l[u] = pl[ii * mstride];
-      o[u] = po[ii * ostride];
+      const bool in = ii < p.P;
+      m[u] = in ? pm[ii * mstride] : -INFINITY;
+      l[u] = in ? pl[ii * mstride] : 0.f;
+      o[u] = in ? po[ii * ostride] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
-      const float f = (m[u] == -INFINITY) ? 0.f : exp2f(m[u] - Mu);
-      L = fmaf(l[u], f, L);
-      acc = fmaf(o[u], f, acc);
+      if (m[u] == -INFINITY) continue;   // an empty partial adds nothing
+      const float Mn = fmaxf(M, m[u]);
+      const float a = (M == Mn) ? 1.f : exp2f(M - Mn);
+      const float w = (m[u] == Mn) ? 1.f : exp2f(m[u] - Mn);
+      L = fmaf(l[u], w, L * a);
+      acc = fmaf(o[u], w, acc * a);
+      M = Mn;
     }
   }
-  for (; i < p.P; i += kMergeWarps) {
-    const float m = pm[i * mstride];
-    const float f = (m == -INFINITY) ? 0.f : exp2f(m - Mu);
-    L = fmaf(pl[i * mstride], f, L);
-    acc = fmaf(po[i * ostride], f, acc);
+  if (lane == 0) {
+    red_m[warp] = M;
+    red_l[warp] = L;
   }
-  if (lane == 0) red_l[warp] = L;
   red_o[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
-    float Lt = 0.f, o = 0.f;
-#pragma unroll
+    float Mt = -INFINITY;
+#pragma unroll 8
+    for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, red_m[w]);
+    float Lt = 0.f, ot = 0.f;
+#pragma unroll 4
     for (int w = 0; w < kMergeWarps; ++w) {
-      Lt += red_l[w];
-      o += red_o[w][lane];
+      const float f = (red_m[w] == -INFINITY) ? 0.f : exp2f(red_m[w] - Mt);
+      Lt = fmaf(red_l[w], f, Lt);
+      ot = fmaf(red_o[w][lane], f, ot);
     }
     const float inv = (Lt > 0.f) ? 1.f / Lt : 0.f;
     const long long od = ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * D + col;
     if (p.out_f32)
-      static_cast<float*>(p.out)[od] = o * inv;
+      static_cast<float*>(p.out)[od] = ot * inv;
     else
-      static_cast<__nv_bfloat16*>(p.out)[od] = __float2bfloat16_rn(o * inv);
+      static_cast<__nv_bfloat16*>(p.out)[od] = __float2bfloat16_rn(ot * inv);
     if (lane == 0 && blockIdx.y == 0 && p.lse != nullptr)
       p.lse[(static_cast<long long>(b) * p.Hq + h) * p.R + tok] =
-          (Lt > 0.f) ? (M + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
+          (Lt > 0.f) ? (Mt + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
   }
 }
 
@@ -544,13 +544,25 @@ int launch_decode(const DecodeParams& p, void* stream) {
     e = (p.D == 128) ? launch_partial<128>(p, grid, s) : launch_partial<64>(p, grid, s);
   }
   if (e != 0) return e;
-  const dim3 mgrid(static_cast<unsigned>(static_cast<long long>(p.B) * p.Hq * p.R),
-                   static_cast<unsigned>(p.D / 32));
+  // The merge may be scheduled while the partial kernel drains; it waits for
+  // that grid's completion (programmatic dependent launch) before reading.
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(p.B) * p.Hq * p.R),
+                     static_cast<unsigned>(p.D / 32));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  std::memset(&attr, 0, sizeof(attr));
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
   launch_stage() = "decode merge kernel launch";
-  if (p.D == 128)
-    decode_merge_kernel<128><<<mgrid, kMergeThreads, 0, s>>>(p);
-  else
-    decode_merge_kernel<64><<<mgrid, kMergeThreads, 0, s>>>(p);
+  const cudaError_t me = (p.D == 128) ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, p)
+                                      : cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, p);
+  if (me != cudaSuccess) return static_cast<int>(me);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -224,6 +224,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
   __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled early
 
   if (warp == kDTWarpLoad) {
     // ===================== TMA loads of the K and V tiles =================
