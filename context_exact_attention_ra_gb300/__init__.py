@@ -263,7 +263,8 @@ def ring_read_work(shape: Shape, c, layout, mode, workspace, stream=None):
 def ring_forward_hostio(q_host, k_host, v_host, c, layout="zigzag", causal=True, mode="fused",
                         scale=None, out_host=None, lse_host=None, workspace=None, stream=None):
     """ring_forward with host (ideally pinned) CPU tensors in and out; the
-    library copies them to and from the device inside the call."""
+    library copies the inputs to the device inside the call, and the kernels
+    write pinned outputs directly (pageable outputs are copied back)."""
     lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     md = MODES[mode] if isinstance(mode, str) else int(mode)
     scale = q_host.shape[-1] ** -0.5 if scale is None else scale

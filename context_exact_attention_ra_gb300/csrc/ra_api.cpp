@@ -689,6 +689,21 @@ size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, in
          round_up(B * S * shp.Hq * D * ob) + round_up(B * shp.Hq * S * sizeof(float));
 }
 
+namespace {
+// The device address of pinned host memory that is mapped into the device's
+// address space (16-byte aligned), else nullptr.
+void* device_view(void* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();   // clear the sticky-free error of an unregistered pointer
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+  if ((reinterpret_cast<uintptr_t>(a.devicePointer) & 15u) != 0) return nullptr;
+  return a.devicePointer;
+}
+}  // namespace
+
 ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const void* v_host,
                                  ra_shape shp, int c, int layout, int causal, int mode,
                                  int out_dtype, void* out_host, float* lse_host, void* workspace,
@@ -716,15 +731,23 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
   void* dout = p; p += round_up(ob);
   float* dlse = reinterpret_cast<float*>(p);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Outputs: when the host buffers are pinned and mapped into the device's
+  // address space, the kernels write them directly (over the CPU-GPU link,
+  // while the attention still runs) instead of a copy after the fact.
+  void* out_dst = device_view(out_host);
+  float* lse_dst = lse_host ? static_cast<float*>(device_view(lse_host)) : nullptr;
+  if (out_dst == nullptr) out_dst = dout;
+  if (lse_host && lse_dst == nullptr) lse_dst = dlse;
   cudaError_t ce = cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s);
   if (ce == cudaSuccess) ce = cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s);
   if (ce == cudaSuccess) ce = cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s);
   if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemcpyAsync (inputs)");
-  st = ra_ring_forward(dq, dk, dv, shp, c, layout, causal, mode, out_dtype, dout,
-                       lse_host ? dlse : nullptr, workspace, base, nullptr, stream);
+  st = ra_ring_forward(dq, dk, dv, shp, c, layout, causal, mode, out_dtype, out_dst, lse_dst, workspace,
+                       base, nullptr, stream);
   if (st != RA_OK) return st;
-  ce = cudaMemcpyAsync(out_host, dout, ob, cudaMemcpyDeviceToHost, s);
-  if (ce == cudaSuccess && lse_host) ce = cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, s);
+  if (out_dst == dout) ce = cudaMemcpyAsync(out_host, dout, ob, cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess && lse_host && lse_dst == dlse)
+    ce = cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, s);
   if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemcpyAsync (outputs)");
   ce = cudaStreamSynchronize(s);
   if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamSynchronize");

@@ -225,7 +225,10 @@ ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const voi
  * memory (pinned for overlap), runs the ring, copies out and lse back, all
  * on `stream`; returns after the stream has finished.  The device buffers
  * for q, k, v, out and lse are carved from the workspace, whose size is
- * ra_ring_forward_hostio_workspace_size(). */
+ * ra_ring_forward_hostio_workspace_size().  When out_host (or lse_host) is
+ * pinned memory mapped into the device's address space, the kernels write it
+ * directly over the CPU-GPU link while they run; otherwise the result is
+ * copied back after the attention. */
 size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode,
                                              int out_dtype);
 ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const void* v_host,

@@ -256,14 +256,18 @@ def test_lse_merge_of_key_splits_equals_full_attention(P):
     parity.check_lse(_np(lse), ref_lse, "merge lse")
 
 
-def test_hostio_equals_device_path():
+# pinned outputs are written by the kernels directly, pageable ones are copied
+@pytest.mark.parametrize("mode,pinned_out", [("fused", True), ("fused", False), ("per_step", True)])
+def test_hostio_equals_device_path(mode, pinned_out):
     w = small_case(2048, 4, "zigzag", True, B=1, Hq=4, Hkv=1, D=128, seed=21)
     q, k, v, _ = make_inputs(w)
-    out_d, lse_d = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, "fused")
+    out_d, lse_d = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, "zigzag", True, mode)
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    out_h = torch.empty_like(qh).pin_memory()
-    lse_h = torch.empty((1, w.Hq, w.S), dtype=torch.float32).pin_memory()
-    ra.ring_forward_hostio(qh, kh, vh, w.c, "zigzag", True, "fused", out_host=out_h, lse_host=lse_h)
+    out_h = torch.empty_like(qh)
+    lse_h = torch.empty((1, w.Hq, w.S), dtype=torch.float32)
+    if pinned_out:
+        out_h, lse_h = out_h.pin_memory(), lse_h.pin_memory()
+    ra.ring_forward_hostio(qh, kh, vh, w.c, "zigzag", True, mode, out_host=out_h, lse_host=lse_h)
     assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
     assert torch.equal(lse_h.view(torch.int32), lse_d.cpu().view(torch.int32))
 
