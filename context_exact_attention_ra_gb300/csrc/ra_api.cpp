@@ -738,12 +738,26 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
   float* lse_dst = lse_host ? static_cast<float*>(device_view(lse_host)) : nullptr;
   if (out_dst == nullptr) out_dst = dout;
   if (lse_host && lse_dst == nullptr) lse_dst = dlse;
-  cudaError_t ce = cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess) ce = cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess) ce = cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s);
+  // Inputs: mapped pinned buffers are read by the shard-pack kernel directly.
+  const void* q_src = device_view(const_cast<void*>(q_host));
+  const void* k_src = device_view(const_cast<void*>(k_host));
+  const void* v_src = device_view(const_cast<void*>(v_host));
+  cudaError_t ce = cudaSuccess;
+  if (q_src == nullptr) {
+    ce = cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s);
+    q_src = dq;
+  }
+  if (ce == cudaSuccess && k_src == nullptr) {
+    ce = cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s);
+    k_src = dk;
+  }
+  if (ce == cudaSuccess && v_src == nullptr) {
+    ce = cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s);
+    v_src = dv;
+  }
   if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemcpyAsync (inputs)");
-  st = ra_ring_forward(dq, dk, dv, shp, c, layout, causal, mode, out_dtype, out_dst, lse_dst, workspace,
-                       base, nullptr, stream);
+  st = ra_ring_forward(q_src, k_src, v_src, shp, c, layout, causal, mode, out_dtype, out_dst, lse_dst,
+                       workspace, base, nullptr, stream);
   if (st != RA_OK) return st;
   if (out_dst == dout) ce = cudaMemcpyAsync(out_host, dout, ob, cudaMemcpyDeviceToHost, s);
   if (ce == cudaSuccess && lse_host && lse_dst == dlse)
