@@ -65,8 +65,8 @@ struct DTSmem {
   static constexpr int bKVEmpty = bKVFull + kDTStages;
   static constexpr int bSFull = bKVEmpty + kDTStages;
   static constexpr int bPFull = bSFull + 2;
-  static constexpr int bPVDone = bPFull + 2;
-  static constexpr int bXch = bPVDone + 1;                   // row-max exchange, 2 parities
+  static constexpr int bPVDone = bPFull + 2;                 // P V of tile j done: [j & 1]
+  static constexpr int bXch = bPVDone + 2;                   // row-max exchange, 2 parities
   static constexpr int bDrain = bXch + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;          // tmem slot, abort flag
@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
       ptx::mbar_init(bar(L::bXch + i), 128);
     }
     ptx::mbar_init(bar(L::bPVDone), 1);
+    ptx::mbar_init(bar(L::bPVDone + 1), 1);
     ptx::mbar_init(bar(L::bDrain), 1);
     *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.err) != 0) ? 1 : 0;
     ptx::fence_mbar_init();
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
           if (!ok) break;
           ptx::tc_fence_after_sync();
           issue_PV((j - 1) % kDTStages, (j - 1) & 1);
-          ptx::tc_commit(bar(L::bPVDone));
+          ptx::tc_commit(bar(L::bPVDone + ((j - 1) & 1)));
           ptx::tc_commit(bar(L::bKVEmpty + (j - 1) % kDTStages));
         }
       }
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         if (ok) {
           ptx::tc_fence_after_sync();
           issue_PV((J - 1) % kDTStages, (J - 1) & 1);
-          ptx::tc_commit(bar(L::bPVDone));
+          ptx::tc_commit(bar(L::bPVDone + ((J - 1) & 1)));
         }
       }
       if (!ok && issued_any) {
@@ -376,7 +377,12 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         any_rescale |= (alpha[n] != 1.f) && (m_run[n] != -INFINITY);
         m_run[n] = m_new;
       }
-      // probabilities: this thread's column of P^T (bf16) and its share of l
+      // probabilities: this thread's column of P^T (bf16) and its share of l;
+      // the buffer was last read by the P V of tile j - 2
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone + sb), ((j - 2) >> 1) & 1u, ab, kErrTimeoutO));
+        if (!ok) break;
+      }
       uint8_t* pbuf = smem + L::kP + sb * L::kPBuf;
 #pragma unroll
       for (int n = 0; n < kDTRows; ++n) {
@@ -388,12 +394,14 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         *reinterpret_cast<__nv_bfloat16*>(pbuf + 2 * L::kRowsBox + off) =
             __float2bfloat16_rn(pr - __bfloat162float(hi));
       }
-      // rescale this thread's column of O^T once the previous P V has run
-      if (j >= 1) {
-        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone), (j - 1) & 1u, ab, kErrTimeoutO));
+      // rescale this thread's column of O^T when a row's maximum rose, once
+      // the previous P V has run (otherwise nothing waits for it)
+      if (j >= 1 && any_rescale) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1u, ab,
+                                              kErrTimeoutO));
         if (!ok) break;
         ptx::tc_fence_after_sync();
-        if (any_rescale) {
+        {
           uint32_t u[16];
           ptx::tmem_ld16(tO, u);
 #pragma unroll
@@ -409,7 +417,8 @@ __global__ void __launch_bounds__(kDTThreads, 1)
 
     // ---- epilogue: the block's partial state ------------------------------
     if (ok && J > 0) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone), (J - 1) & 1u, ab, kErrTimeoutO));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone + ((J - 1) & 1)), ((J - 1) >> 1) & 1u, ab,
+                                            kErrTimeoutO));
       if (ok) ptx::tc_fence_after_sync();
     }
     if (ok) {
