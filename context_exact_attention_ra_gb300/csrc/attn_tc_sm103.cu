@@ -530,29 +530,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         uint32_t sv[128];
-        ptx::tmem_ld128(tS, sv);
-        if (masked) {
+        float mx;
+        if (!masked) {
+          // every key visible: the tensor-memory load itself forms the row
+          // maximum (tcgen05.ld.red, sm_103a)
+          ptx::tmem_ld128_max(tS, sv, mx);
+        } else {
+          ptx::tmem_ld128(tS, sv);
           // hidden or padding keys become -inf before the max and the exponent
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (!((bits[i >> 5] >> (i & 31)) & 1u)) sv[i] = 0xff800000u;
-        }
-        // row maximum: eight independent chains of three-input max
-        float mc[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          mc[c] = ptx::fmax3(__uint_as_float(sv[16 * c]), __uint_as_float(sv[16 * c + 1]),
-                             __uint_as_float(sv[16 * c + 2]));
-#pragma unroll
-        for (int i = 3; i < 15; i += 2) {
+          // row maximum: eight independent chains of three-input max
+          float mc[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            mc[c] = ptx::fmax3(mc[c], __uint_as_float(sv[16 * c + i]), __uint_as_float(sv[16 * c + i + 1]));
-        }
+            mc[c] = ptx::fmax3(__uint_as_float(sv[16 * c]), __uint_as_float(sv[16 * c + 1]),
+                               __uint_as_float(sv[16 * c + 2]));
 #pragma unroll
-        for (int c = 0; c < 8; ++c) mc[c] = fmaxf(mc[c], __uint_as_float(sv[16 * c + 15]));
-        const float mx = ptx::fmax3(ptx::fmax3(mc[0], mc[1], mc[2]), ptx::fmax3(mc[3], mc[4], mc[5]),
-                                    fmaxf(mc[6], mc[7]));
+          for (int i = 3; i < 15; i += 2) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              mc[c] = ptx::fmax3(mc[c], __uint_as_float(sv[16 * c + i]), __uint_as_float(sv[16 * c + i + 1]));
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) mc[c] = fmaxf(mc[c], __uint_as_float(sv[16 * c + 15]));
+          mx = ptx::fmax3(ptx::fmax3(mc[0], mc[1], mc[2]), ptx::fmax3(mc[3], mc[4], mc[5]),
+                          fmaxf(mc[6], mc[7]));
+        }
         const float m_new = fmaxf(m_run, mx * sl2);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
