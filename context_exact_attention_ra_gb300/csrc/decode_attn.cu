@@ -41,8 +41,8 @@ constexpr int kSub = 16;         // keys per warp step: the MMA's K for P V
 constexpr int kPiece = 128;      // shard-local keys per piece
 constexpr int kTargetBlocks = 304;   // two resident blocks on each of 152 SMs
 constexpr int kStages = 3;           // staged 16-key chunks per warp (two loads in flight)
-constexpr int kMergeWarps = 32;
-constexpr int kMergeUnroll = 5;     // partial loads in flight per lane
+constexpr int kMergeWarps = 16;   // 56 registers x 512 threads: fits beside a partial block
+constexpr int kMergeUnroll = 10;    // partial loads in flight per lane
 constexpr int kMergeThreads = kMergeWarps * 32;
 
 template <int D>
@@ -427,14 +427,16 @@ __global__ void __launch_bounds__(kDecThreads)
   }
 }
 
-// One block of 32 warps per (b, h, token) and 32-column slice of the head
+// One block of 16 warps per (b, h, token) and 32-column slice of the head
 // dimension: merge the P partials, normalise, write out (and, from the first
-// slice, lse).  Lane = column; the warps take every 32nd partial (five loads
+// slice, lse).  Lane = column; the warps take every 16th partial (ten loads
 // in flight) and fold them in one online pass; the warps' states are then
-// combined in warp order.  Launched as a dependent of the partial kernel: it
-// waits for that grid to finish before it reads the partials.
+// combined, each warp's weight computed by one lane.  Launched as a dependent
+// of the partial kernel: the block is small enough to become resident beside
+// a partial block, and waits for that grid to finish before it reads the
+// partials.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
+__global__ void __maxnreg__(56) decode_merge_kernel(const DecodeParams p) {
   __shared__ float red_m[kMergeWarps];
   __shared__ float red_l[kMergeWarps];
   __shared__ float red_o[kMergeWarps][32];
@@ -452,23 +454,28 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const float* pl = p.part_l + (static_cast<long long>(b) * p.Hq + h) * p.R + tok;
   const float* po = p.part_o + ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * D + col;
   float M = -INFINITY, L = 0.f, acc = 0.f;
+  static_assert(kMergeUnroll <= 16, "m and l of a round are fetched by lanes 0-15 and 16-31");
   for (int i = warp; i < p.P; i += kMergeUnroll * kMergeWarps) {
-    float m[kMergeUnroll], l[kMergeUnroll], o[kMergeUnroll];
+    // lane u (< 16) fetches m of the round's partial u, lane 16 + u its l
+    const int u_ld = lane & 15;
+    const long long i_ld = i + static_cast<long long>(u_ld) * kMergeWarps;
+    float ml = (lane < 16) ? -INFINITY : 0.f;
+    if (u_ld < kMergeUnroll && i_ld < p.P) ml = (lane < 16) ? pm[i_ld * mstride] : pl[i_ld * mstride];
+    float o[kMergeUnroll];
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
       const long long ii = i + u * kMergeWarps;
-      const bool in = ii < p.P;
-      m[u] = in ? pm[ii * mstride] : -INFINITY;
-      l[u] = in ? pl[ii * mstride] : 0.f;
-      o[u] = in ? po[ii * ostride] : 0.f;
+      o[u] = (ii < p.P) ? po[ii * ostride] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
-      if (m[u] == -INFINITY) continue;   // an empty partial adds nothing
-      const float Mn = fmaxf(M, m[u]);
+      const float mu = __shfl_sync(0xffffffffu, ml, u);
+      const float lu = __shfl_sync(0xffffffffu, ml, 16 + u);
+      if (mu == -INFINITY) continue;   // an empty partial adds nothing
+      const float Mn = fmaxf(M, mu);
       const float a = (M == Mn) ? 1.f : exp2f(M - Mn);
-      const float w = (m[u] == Mn) ? 1.f : exp2f(m[u] - Mn);
-      L = fmaf(l[u], w, L * a);
+      const float w = (mu == Mn) ? 1.f : exp2f(mu - Mn);
+      L = fmaf(lu, w, L * a);
       acc = fmaf(o[u], w, acc * a);
       M = Mn;
     }
@@ -480,16 +487,19 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   red_o[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
-    float Mt = -INFINITY;
-#pragma unroll 8
-    for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, red_m[w]);
-    float Lt = 0.f, ot = 0.f;
-#pragma unroll 4
-    for (int w = 0; w < kMergeWarps; ++w) {
-      const float f = (red_m[w] == -INFINITY) ? 0.f : exp2f(red_m[w] - Mt);
-      Lt = fmaf(red_l[w], f, Lt);
-      ot = fmaf(red_o[w][lane], f, ot);
-    }
+    // lane w < kMergeWarps holds warp w's state: the block maximum by
+    // shuffles, warp w's weight f, and l summed over the warps
+    const float mw = (lane < kMergeWarps) ? red_m[lane] : -INFINITY;
+    float Mt = mw;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Mt = fmaxf(Mt, __shfl_xor_sync(0xffffffffu, Mt, o));
+    const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - Mt);
+    float Lt = (lane < kMergeWarps) ? red_l[lane] * f : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
+    float ot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) ot = fmaf(red_o[w][lane], __shfl_sync(0xffffffffu, f, w), ot);
     const float inv = (Lt > 0.f) ? 1.f / Lt : 0.f;
     const long long od = ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * D + col;
     if (p.out_f32)

@@ -16,7 +16,11 @@
 // 128 threads (shuffles, then four warps through shared memory), it writes its
 // 16 probabilities into the P^T operand as a bf16 head plus a bf16 remainder
 // (so P enters the product with about 16 bits, and the result stays within
-// 1e-4 of the float64 definition) and keeps its own share of the row sums; every thread also owns one output column of O^T and rescales it
+// 1e-4 of the float64 definition) and keeps its own share of the row sums.
+// Heads and remainders are stacked as the operand's 32 rows, so one N = 32
+// product per 16 keys accumulates both into separate columns of O^T (an
+// instruction costs the tensor core the same for any N up to 128), added in
+// the epilogue.  Every thread also owns one output column of O^T and rescales it
 // when a row's maximum rose.  K and V tiles stream through three shared-memory
 // stages by TMA, so the block reads each key and value byte once, and the
 // kernel is bound by HBM bandwidth.
@@ -47,7 +51,7 @@ constexpr int kDTStages = 3;
 constexpr int kDTWarpLoad = 4;
 constexpr int kDTWarpMma = 5;
 constexpr int kDTThreads = 6 * 32;
-constexpr uint32_t kDTTmemCols = 64;  // S0 | S1 | O, 16 columns each
+constexpr uint32_t kDTTmemCols = 64;  // S0 | S1 | O heads | O remainders, 16 columns each
 constexpr int kDTTargetBlocks = 152;  // one resident block per SM
 
 struct DTSmem {
@@ -56,7 +60,8 @@ struct DTSmem {
   static constexpr int kKVTile = 2 * kKVBox;                 // 32 KB: 128 keys x 128 columns
   static constexpr int kRowsBox = kDTRows * kBox * 2;        // 2 KB: 16 rows x 64 columns
   static constexpr int kQ = 0;                               // Q: 16 rows x 128 columns (2 boxes)
-  static constexpr int kPBuf = 2 * 2 * kRowsBox;             // P^T head and remainder, 16 x 128 each
+  static constexpr int kPBox = 2 * kRowsBox;                 // 4 KB: 32 rows (16 heads, 16 remainders) x 64 keys
+  static constexpr int kPBuf = 2 * kPBox;                    // P^T for the 128 keys of a tile
   static constexpr int kP = kQ + 2 * kRowsBox;               // two such buffers
   static constexpr int kK = kP + 2 * kPBuf;
   static constexpr int kV = kK + kDTStages * kKVTile;
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
     // ===================== tensor-core issue ============================
     if (lane == 0) {
       constexpr uint32_t idS = ptx::idesc_bf16_f32(128, kDTRows, false, false);
-      constexpr uint32_t idPV = ptx::idesc_bf16_f32(128, kDTRows, false, true);
+      constexpr uint32_t idPV = ptx::idesc_bf16_f32(128, 2 * kDTRows, false, true);
       const uint64_t dQ = ptx::smem_desc_sw128(sbase + L::kQ, 16, 1024);
       const uint64_t dK = ptx::smem_desc_sw128(sbase + L::kK, 16, 1024);
       const uint64_t dV = ptx::smem_desc_sw128(sbase + L::kV, L::kKVBox, 1024);
@@ -279,15 +284,13 @@ __global__ void __launch_bounds__(kDTThreads, 1)
       };
       auto issue_PV = [&](int st, int pb) {
         const uint64_t vd = dV + static_cast<uint64_t>((st * L::kKVTile) >> 4);
+        const uint64_t pd = dP + static_cast<uint64_t>((pb * L::kPBuf) >> 4);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {   // bf16 head of P, then its remainder
-          const uint64_t pd = dP + static_cast<uint64_t>((pb * L::kPBuf + part * 2 * L::kRowsBox) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kDTKeys / 16; ++kk) {
-            const uint64_t oa = static_cast<uint64_t>((kk * 16 * 128) >> 4);
-            const uint64_t ob = static_cast<uint64_t>(((kk / 4) * L::kRowsBox + (kk % 4) * 32) >> 4);
-            ptx::tc_mma_ss(tmem + 2 * kDTRows, vd + oa, pd + ob, idPV, 1u);
-          }
+        for (int kk = 0; kk < kDTKeys / 16; ++kk) {
+          // N = 32: the heads of P into O's first 16 columns, the remainders into the next 16
+          const uint64_t oa = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+          const uint64_t ob = static_cast<uint64_t>(((kk / 4) * L::kPBox + (kk % 4) * 32) >> 4);
+          ptx::tc_mma_ss(tmem + 2 * kDTRows, vd + oa, pd + ob, idPV, 1u);
         }
       };
       for (int j = 0; j < J && ok; ++j) {
@@ -327,10 +330,10 @@ __global__ void __launch_bounds__(kDTThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tO = tmem + lane_base + 2 * kDTRows;
     {
-      uint32_t z[16];
+      uint32_t z[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) z[i] = 0u;
-      ptx::tmem_st16(tO, z);
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+      ptx::tmem_st32(tO, z);
       ptx::tmem_wait_st();
     }
     float m_run[kDTRows], lpart[kDTRows];
@@ -389,9 +392,8 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         const float pr = (x[n] == -INFINITY) ? 0.f : ptx::ex2(x[n] - muse[n]);
         lpart[n] = lpart[n] * alpha[n] + pr;
         const __nv_bfloat16 hi = __float2bfloat16_rn(pr);
-        const uint32_t off = sw128_offset(n, t, L::kRowsBox);
-        *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(pbuf + 2 * L::kRowsBox + off) =
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128_offset(n, t, L::kPBox)) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128_offset(kDTRows + n, t, L::kPBox)) =
             __float2bfloat16_rn(pr - __bfloat162float(hi));
       }
       // rescale this thread's column of O^T when a row's maximum rose, once
@@ -402,11 +404,14 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         if (!ok) break;
         ptx::tc_fence_after_sync();
         {
-          uint32_t u[16];
-          ptx::tmem_ld16(tO, u);
+          uint32_t u[32];
+          ptx::tmem_ld32(tO, u);
 #pragma unroll
-          for (int n = 0; n < kDTRows; ++n) u[n] = __float_as_uint(__uint_as_float(u[n]) * alpha[n]);
-          ptx::tmem_st16(tO, u);
+          for (int n = 0; n < kDTRows; ++n) {
+            u[n] = __float_as_uint(__uint_as_float(u[n]) * alpha[n]);
+            u[kDTRows + n] = __float_as_uint(__uint_as_float(u[kDTRows + n]) * alpha[n]);
+          }
+          ptx::tmem_st32(tO, u);
           ptx::tmem_wait_st();
         }
       }
@@ -429,8 +434,8 @@ __global__ void __launch_bounds__(kDTThreads, 1)
       ptx::mbar_arrive(bar(L::bXch + (J & 1)));
       ok = __all_sync(0xffffffffu, wait_bar(bar(L::bXch + (J & 1)), (J >> 1) & 1u, ab, kErrTimeoutS));
       if (ok) {
-        uint32_t u[16];
-        ptx::tmem_ld16(tO, u);
+        uint32_t u[32];
+        ptx::tmem_ld32(tO, u);
 #pragma unroll
         for (int n = 0; n < kDTRows; ++n) {
           if (n >= nrows) break;
@@ -439,7 +444,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
           const int tok = rr % p.R;
           // partial layout: o [P, B, R, Hq, D]; m, l [P, B, Hq, R]
           p.part_o[(((static_cast<long long>(pi) * p.B + b) * p.R + tok) * p.Hq + h) * kDTD + t] =
-              __uint_as_float(u[n]);
+              __uint_as_float(u[n]) + __uint_as_float(u[kDTRows + n]);
         }
         if (t < nrows) {
           const int n = t;
