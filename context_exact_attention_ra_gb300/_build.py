@@ -4,7 +4,7 @@ Every CUDA source is compiled for sm_103a only (``-gencode
 arch=compute_103a,code=sm_103a``), host sources with the same nvcc driver;
 translation units compile in parallel and link into one shared object with
 the static CUDA runtime, so the library depends on no CUDA shared object at
-load time (the driver is looked up through the runtime when first needed).
+load time (the CUDA driver API is looked up through the runtime when first needed).
 """
 
 from __future__ import annotations

@@ -1,5 +1,5 @@
 // Host side of the TMA loads: tensor maps over [B][rows][H][D] bf16 tensors.
-// The driver's cuTensorMapEncodeTiled is looked up once through the runtime.
+// The CUDA driver API's cuTensorMapEncodeTiled is looked up once through the runtime.
 
 #include <cuda.h>
 #include <cuda_runtime.h>

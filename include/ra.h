@@ -58,7 +58,7 @@ typedef struct CUstream_st* ra_stream_t;
 typedef enum {
   RA_OK = 0,
   RA_ERR_INVALID = -1,      /* an argument is out of range, null or misaligned */
-  RA_ERR_UNSUPPORTED = -2,  /* valid request this build does not implement   */
+  RA_ERR_UNSUPPORTED = -2,  /* valid request the library does not implement  */
   RA_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed              */
   RA_ERR_TIMEOUT = -4,      /* a bounded device-side wait ran out             */
   RA_ERR_WORKSPACE = -5     /* workspace missing or smaller than required     */
