@@ -126,105 +126,101 @@ struct MergeParams {
 // One warp per kMergeRows rows of (b, s, h), h fastest -- the order of the
 // partial outputs in memory, so a warp reads one contiguous stretch and
 // neighbouring warps the next ones; lanes hold D/32 consecutive columns of
-// each row.  One online pass over the partials: per
-// partial the warp issues all its rows' loads before using any of them, and
+// each row, and one lane per row fetches its m (another its l), so that
+// four rows with two partials in flight fit three blocks per SM.  One online
+// pass over the partials: per partial the warp issues all its rows' loads
+// before using any of them, and
 //   M' = max(M, m_p),  L' = 2^(M - M') L + 2^(m_p - M') l_p,
 //   acc' = 2^(M - M') acc + 2^(m_p - M') o_p            (base-2 units).
 // For a single partial the weights are exactly 1, so out = o / l bit for bit
 // as in the fused kernel's epilogue.
-constexpr int kMergeRows = 2;
+constexpr int kMergeRows = 4;
 
 template <int D>
-__global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams mp) {
+__global__ void __launch_bounds__(256, 3) merge_kernel(const MergeParams mp) {
   constexpr int V = D / 32;   // floats per lane
+  constexpr int R = kMergeRows;
   const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(mp.B) * mp.Hq * mp.S;
-  const long long row0 = warp_id * kMergeRows;
+  const long long row0 = warp_id * R;
   if (row0 >= rows) return;
-  long long si[kMergeRows], oi[kMergeRows];
-  int bb[kMergeRows], hh[kMergeRows], ss[kMergeRows];
-  bool live[kMergeRows];
-  // (b, s, h) of the first row by division, of the others by stepping h
-  const long long q0 = row0 / mp.Hq;
-  int h = static_cast<int>(row0 - q0 * mp.Hq);
-  int sidx = static_cast<int>(q0 % mp.S);
-  int bidx = static_cast<int>(q0 / mp.S);
+  // Lane r < R owns row r's m, lane R + r its l: (b, s, h) of that row and
+  // the index of its m and l in [B, Hq, S]; the values reach the other lanes
+  // by shuffles.
+  const long long my_row = min(row0 + (lane % R), rows - 1);
+  const long long q0 = my_row / mp.Hq;
+  const int my_h = static_cast<int>(my_row - q0 * mp.Hq);
+  const int my_s = static_cast<int>(q0 % mp.S);
+  const int my_b = static_cast<int>(q0 / mp.S);
+  const long long my_si = (static_cast<long long>(my_b) * mp.Hq + my_h) * mp.S + my_s;
+  const bool ml_lane = lane < 2 * R;
+  const long long obase = row0 * D + lane * V;   // o is [B, S, Hq, D]: these rows are consecutive
+  const int nlive = static_cast<int>(min(static_cast<long long>(R), rows - row0));
+
+  float M[R], L[R], acc[R][V];
 #pragma unroll
-  for (int r = 0; r < kMergeRows; ++r) {
-    const long long row = row0 + r;
-    live[r] = row < rows;
-    hh[r] = live[r] ? h : hh[0];
-    ss[r] = live[r] ? sidx : ss[0];
-    bb[r] = live[r] ? bidx : bb[0];
-    si[r] = (static_cast<long long>(bb[r]) * mp.Hq + hh[r]) * mp.S + ss[r];
-    oi[r] = (live[r] ? row : row0) * D + lane * V;   // o is [B, S, Hq, D]: rows in this order are consecutive
-    if (++h == mp.Hq) {
-      h = 0;
-      if (++sidx == mp.S) {
-        sidx = 0;
-        ++bidx;
-      }
-    }
-  }
-  float M[kMergeRows], L[kMergeRows], acc[kMergeRows][V];
-#pragma unroll
-  for (int r = 0; r < kMergeRows; ++r) {
+  for (int r = 0; r < R; ++r) {
     M[r] = -INFINITY;
     L[r] = 0.f;
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[r][i] = 0.f;
   }
-  // The loads of partial pi + 1 are issued before partial pi is folded in.
-  float mv[kMergeRows], lv[kMergeRows], ov[kMergeRows][V];
-  auto load = [&](int pi, float (&m_)[kMergeRows], float (&l_)[kMergeRows], float (&o_)[kMergeRows][V]) {
-    const float* mpp = mp.a.ms[pi];
-    const float* lpp = mp.a.ls[pi];
-    const float* opp = mp.a.outs[pi];
+  auto load = [&](int pi, float& ml_, float (&o_)[R][V]) {
+    ml_ = ml_lane ? __ldg((lane < R ? mp.a.ms[pi] : mp.a.ls[pi]) + my_si) : 0.f;
+    const float* opp = mp.a.outs[pi] + obase;
 #pragma unroll
-    for (int r = 0; r < kMergeRows; ++r) {
-      m_[r] = __ldg(mpp + si[r]);
-      l_[r] = __ldg(lpp + si[r]);
-      if constexpr (V == 4) {
-        const float4 f = __ldcs(reinterpret_cast<const float4*>(opp + oi[r]));
-        o_[r][0] = f.x; o_[r][1] = f.y; o_[r][2] = f.z; o_[r][3] = f.w;
+    for (int r = 0; r < R; ++r) {
+      if (r < nlive) {
+        if constexpr (V == 4) {
+          const float4 f = __ldcs(reinterpret_cast<const float4*>(opp + r * D));
+          o_[r][0] = f.x; o_[r][1] = f.y; o_[r][2] = f.z; o_[r][3] = f.w;
+        } else {
+          const float2 f = __ldcs(reinterpret_cast<const float2*>(opp + r * D));
+          o_[r][0] = f.x; o_[r][1] = f.y;
+        }
       } else {
-        const float2 f = __ldcs(reinterpret_cast<const float2*>(opp + oi[r]));
-        o_[r][0] = f.x; o_[r][1] = f.y;
+#pragma unroll
+        for (int i = 0; i < V; ++i) o_[r][i] = 0.f;
       }
     }
   };
-  load(0, mv, lv, ov);
+  // The loads of partial pi + 1 are issued before partial pi is folded in.
+  float mlv, ov[R][V];
+  load(0, mlv, ov);
   for (int pi = 0; pi < mp.a.P; ++pi) {
-    float mn[kMergeRows], ln[kMergeRows], on[kMergeRows][V];
-    if (pi + 1 < mp.a.P) load(pi + 1, mn, ln, on);
+    float mln, on[R][V];
+    if (pi + 1 < mp.a.P) load(pi + 1, mln, on);
 #pragma unroll
-    for (int r = 0; r < kMergeRows; ++r) {
-      if (mv[r] == -INFINITY) continue;   // an empty partial adds nothing
-      const float Mn = fmaxf(M[r], mv[r]);
+    for (int r = 0; r < R; ++r) {
+      const float mv = __shfl_sync(0xffffffffu, mlv, r);
+      const float lv = __shfl_sync(0xffffffffu, mlv, R + r);
+      if (mv == -INFINITY) continue;   // an empty partial adds nothing
+      const float Mn = fmaxf(M[r], mv);
       const float alpha = (M[r] == Mn) ? 1.f : exp2f(M[r] - Mn);
-      const float w = (mv[r] == Mn) ? 1.f : exp2f(mv[r] - Mn);
-      L[r] = fmaf(lv[r], w, L[r] * alpha);
+      const float w = (mv == Mn) ? 1.f : exp2f(mv - Mn);
+      L[r] = fmaf(lv, w, L[r] * alpha);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[r][i] = fmaf(ov[r][i], w, acc[r][i] * alpha);
       M[r] = Mn;
     }
     if (pi + 1 < mp.a.P) {
+      mlv = mln;
 #pragma unroll
-      for (int r = 0; r < kMergeRows; ++r) {
-        mv[r] = mn[r];
-        lv[r] = ln[r];
+      for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int i = 0; i < V; ++i) ov[r][i] = on[r][i];
-      }
     }
   }
 #pragma unroll
-  for (int r = 0; r < kMergeRows; ++r) {
-    if (!live[r]) continue;
+  for (int r = 0; r < R; ++r) {
+    const int hh = __shfl_sync(0xffffffffu, my_h, r);
+    const int ss = __shfl_sync(0xffffffffu, my_s, r);
+    const int bb = __shfl_sync(0xffffffffu, my_b, r);
+    if (r >= nlive) continue;
     const float inv = (L[r] > 0.f) ? 1.f / L[r] : 0.f;
-    const int orow = (mp.out_row != nullptr) ? mp.out_row[ss[r]] : ss[r];
-    const long long od = ((static_cast<long long>(bb[r]) * mp.S_out + orow) * mp.Hq + hh[r]) * D + lane * V;
+    const int orow = (mp.out_row != nullptr) ? mp.out_row[ss] : ss;
+    const long long od = ((static_cast<long long>(bb) * mp.S_out + orow) * mp.Hq + hh) * D + lane * V;
     if (mp.out_dtype == RA_F32) {
       float* o = static_cast<float*>(mp.out) + od;
       if constexpr (V == 4)
@@ -246,7 +242,7 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams mp) {
       }
     }
     if (lane == 0 && mp.lse != nullptr)
-      mp.lse[(static_cast<long long>(bb[r]) * mp.Hq + hh[r]) * mp.S_out + orow] =
+      mp.lse[(static_cast<long long>(bb) * mp.Hq + hh) * mp.S_out + orow] =
           (L[r] > 0.f) ? (M[r] + log2f(L[r])) * 0.69314718055994531f : -INFINITY;
   }
 }
