@@ -251,51 +251,47 @@ __global__ void __launch_bounds__(256, 3) merge_kernel(const MergeParams mp) {
 // lse = m + log2 l, with m in base-2 units -- the fused kernel's epilogue
 // arithmetic, so both modes agree bit for bit.  Each thread owns one 16-byte
 // slice of kFinRows consecutive rows ((b, s, h) with h fastest, the order of o
-// in memory) and issues all their loads before using any.
-constexpr int kFinRows = 4;
+// in memory) and issues all their loads before using any; a row's m and l are
+// fetched once per group of lanes, which leaves eight rows (128 bytes of loads
+// per thread) within 64 registers, four blocks per SM.
+constexpr int kFinRows = 8;
 
 template <int D>
-__global__ void __launch_bounds__(256) finalize_kernel(const MergeParams mp) {
-  constexpr int C = D / 4;   // float4 slices per row
+__global__ void __launch_bounds__(256, 4) finalize_kernel(const MergeParams mp) {
+  constexpr int C = D / 4;   // float4 slices per row: the lanes of a group
+  static_assert(2 * kFinRows <= C, "m and l of a group's rows are fetched by its first 2 kFinRows lanes");
   const long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   const long long rows = static_cast<long long>(mp.B) * mp.Hq * mp.S;
   const int c4 = static_cast<int>(t % C);
   const long long row0 = (t / C) * kFinRows;
-  if (row0 >= rows) return;
+  if (row0 >= rows) return;   // whole groups of C lanes leave together
   const float* o = mp.a.outs[0];
-  const float* m = mp.a.ms[0];
-  const float* l = mp.a.ls[0];
-  const long long q0 = row0 / mp.Hq;
-  int h = static_cast<int>(row0 - q0 * mp.Hq);
-  int sidx = static_cast<int>(q0 % mp.S);
-  int bidx = static_cast<int>(q0 / mp.S);
+  // lane c4 < kFinRows owns row row0 + c4: its (b, s, h) and its m; lane
+  // kFinRows + c4 the same row's l; the values reach the group by shuffles
+  const long long my_row = min(row0 + (c4 % kFinRows), rows - 1);
+  const long long q0 = my_row / mp.Hq;
+  const int my_h = static_cast<int>(my_row - q0 * mp.Hq);
+  const int my_s = static_cast<int>(q0 % mp.S);
+  const int my_b = static_cast<int>(q0 / mp.S);
+  const long long my_si = (static_cast<long long>(my_b) * mp.Hq + my_h) * mp.S + my_s;
+  const float ml = (c4 < 2 * kFinRows) ? (c4 < kFinRows ? mp.a.ms[0] : mp.a.ls[0])[my_si] : 0.f;
   float4 ov[kFinRows];
-  float mv[kFinRows], lv[kFinRows];
-  int hh[kFinRows], ss[kFinRows], bb[kFinRows];
+#pragma unroll
+  for (int r = 0; r < kFinRows; ++r)
+    ov[r] = (row0 + r < rows) ? __ldcs(reinterpret_cast<const float4*>(o + (row0 + r) * D) + c4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+  const unsigned gmask = (C == 32) ? 0xffffffffu : (0xffffu << (threadIdx.x & 16));
 #pragma unroll
   for (int r = 0; r < kFinRows; ++r) {
-    const bool live = row0 + r < rows;
-    hh[r] = h;
-    ss[r] = sidx;
-    bb[r] = bidx;
-    const long long si = (static_cast<long long>(bidx) * mp.Hq + h) * mp.S + sidx;
-    ov[r] = live ? __ldcs(reinterpret_cast<const float4*>(o + (row0 + r) * D) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    mv[r] = live ? m[si] : 0.f;
-    lv[r] = live ? l[si] : 0.f;
-    if (++h == mp.Hq) {
-      h = 0;
-      if (++sidx == mp.S) {
-        sidx = 0;
-        ++bidx;
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < kFinRows; ++r) {
+    const float mv = __shfl_sync(gmask, ml, r, C);
+    const float lv = __shfl_sync(gmask, ml, kFinRows + r, C);
+    const int hh = __shfl_sync(gmask, my_h, r, C);
+    const int ss = __shfl_sync(gmask, my_s, r, C);
+    const int bb = __shfl_sync(gmask, my_b, r, C);
     if (row0 + r >= rows) break;
-    const float inv = (lv[r] > 0.f) ? 1.f / lv[r] : 0.f;
-    const int orow = (mp.out_row != nullptr) ? mp.out_row[ss[r]] : ss[r];
-    const long long od = ((static_cast<long long>(bb[r]) * mp.S_out + orow) * mp.Hq + hh[r]) * D + c4 * 4;
+    const float inv = (lv > 0.f) ? 1.f / lv : 0.f;
+    const int orow = (mp.out_row != nullptr) ? mp.out_row[ss] : ss;
+    const long long od = ((static_cast<long long>(bb) * mp.S_out + orow) * mp.Hq + hh) * D + c4 * 4;
     if (mp.out_dtype == RA_F32) {
       *reinterpret_cast<float4*>(static_cast<float*>(mp.out) + od) =
           make_float4(ov[r].x * inv, ov[r].y * inv, ov[r].z * inv, ov[r].w * inv);
@@ -308,8 +304,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(const MergeParams mp) {
       *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(mp.out) + od) = w;
     }
     if (c4 == 0 && mp.lse != nullptr)
-      mp.lse[(static_cast<long long>(bb[r]) * mp.Hq + hh[r]) * mp.S_out + orow] =
-          (lv[r] > 0.f) ? (mv[r] + log2f(lv[r])) * 0.69314718055994531f : -INFINITY;
+      mp.lse[(static_cast<long long>(bb) * mp.Hq + hh) * mp.S_out + orow] =
+          (lv > 0.f) ? (mv + log2f(lv)) * 0.69314718055994531f : -INFINITY;
   }
 }
 
