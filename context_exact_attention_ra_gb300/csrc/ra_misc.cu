@@ -126,49 +126,55 @@ struct MergeParams {
 // One warp per kMergeRows rows of (b, s, h), h fastest -- the order of the
 // partial outputs in memory, so a warp reads one contiguous stretch and
 // neighbouring warps the next ones; lanes hold D/32 consecutive columns of
-// each row, and one lane per row fetches its m (another its l), so that
-// four rows with two partials in flight fit three blocks per SM.  One online
-// pass over the partials: per partial the warp issues all its rows' loads
-// before using any of them, and
-//   M' = max(M, m_p),  L' = 2^(M - M') L + 2^(m_p - M') l_p,
-//   acc' = 2^(M - M') acc + 2^(m_p - M') o_p            (base-2 units).
-// For a single partial the weights are exactly 1, so out = o / l bit for bit
-// as in the fused kernel's epilogue.
+// each row.  Two passes: first every partial's m and l (one lane per
+// (partial, row) pair) give the row maximum M = max_p m_p, the weights
+// w_p = 2^(m_p - M) and L = sum_p w_p l_p (base-2 units); then the o rows are
+// summed, acc = sum_p w_p o_p, with the next partial's loads issued before the
+// current one is added -- no exponential between two partials' loads.
+// out = acc / L, lse = ln 2 (M + log2 L).
 constexpr int kMergeRows = 4;
 
 template <int D>
-__global__ void __launch_bounds__(256, 3) merge_kernel(const MergeParams mp) {
+__global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams mp) {
   constexpr int V = D / 32;   // floats per lane
   constexpr int R = kMergeRows;
+  constexpr int PC = 32 / R;  // partials whose weights one pass of the lanes covers
   const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(mp.B) * mp.Hq * mp.S;
   const long long row0 = warp_id * R;
   if (row0 >= rows) return;
-  // Lane r < R owns row r's m, lane R + r its l: (b, s, h) of that row and
-  // the index of its m and l in [B, Hq, S]; the values reach the other lanes
-  // by shuffles.
-  const long long my_row = min(row0 + (lane % R), rows - 1);
+  // lane = pl * R + r holds partial (p0 + pl) of row r: (b, s, h) of row r and
+  // the index of its m and l in [B, Hq, S]
+  const int my_r = lane % R;
+  const int my_pl = lane / R;
+  const long long my_row = min(row0 + my_r, rows - 1);
   const long long q0 = my_row / mp.Hq;
   const int my_h = static_cast<int>(my_row - q0 * mp.Hq);
   const int my_s = static_cast<int>(q0 % mp.S);
   const int my_b = static_cast<int>(q0 / mp.S);
   const long long my_si = (static_cast<long long>(my_b) * mp.Hq + my_h) * mp.S + my_s;
-  const bool ml_lane = lane < 2 * R;
   const long long obase = row0 * D + lane * V;   // o is [B, S, Hq, D]: these rows are consecutive
   const int nlive = static_cast<int>(min(static_cast<long long>(R), rows - row0));
+  const int P = mp.a.P;
 
-  float M[R], L[R], acc[R][V];
+  // pass 1: row maximum over the partials (lanes of one row: lane % R equal)
+  float Mx = -INFINITY;
+  for (int p0 = 0; p0 < P; p0 += PC) {
+    const int p = p0 + my_pl;
+    if (p < P) Mx = fmaxf(Mx, __ldg(mp.a.ms[p] + my_si));
+  }
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    M[r] = -INFINITY;
-    L[r] = 0.f;
+  for (int o = R; o < 32; o <<= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+
+  float acc[R][V];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[r][i] = 0.f;
-  }
-  auto load = [&](int pi, float& ml_, float (&o_)[R][V]) {
-    ml_ = ml_lane ? __ldg((lane < R ? mp.a.ms[pi] : mp.a.ls[pi]) + my_si) : 0.f;
-    const float* opp = mp.a.outs[pi] + obase;
+  float Lsum = 0.f;   // this lane's share of L for row my_r
+  auto load = [&](int p, float (&o_)[R][V]) {
+    const float* opp = mp.a.outs[p] + obase;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       if (r < nlive) {
@@ -185,40 +191,46 @@ __global__ void __launch_bounds__(256, 3) merge_kernel(const MergeParams mp) {
       }
     }
   };
-  // The loads of partial pi + 1 are issued before partial pi is folded in.
-  float mlv, ov[R][V];
-  load(0, mlv, ov);
-  for (int pi = 0; pi < mp.a.P; ++pi) {
-    float mln, on[R][V];
-    if (pi + 1 < mp.a.P) load(pi + 1, mln, on);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float mv = __shfl_sync(0xffffffffu, mlv, r);
-      const float lv = __shfl_sync(0xffffffffu, mlv, R + r);
-      if (mv == -INFINITY) continue;   // an empty partial adds nothing
-      const float Mn = fmaxf(M[r], mv);
-      const float alpha = (M[r] == Mn) ? 1.f : exp2f(M[r] - Mn);
-      const float w = (mv == Mn) ? 1.f : exp2f(mv - Mn);
-      L[r] = fmaf(lv, w, L[r] * alpha);
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[r][i] = fmaf(ov[r][i], w, acc[r][i] * alpha);
-      M[r] = Mn;
+  float ov[R][V];
+  load(0, ov);
+  for (int p0 = 0; p0 < P; p0 += PC) {
+    // pass 2 for partials p0 .. p0 + PC - 1: this lane's weight and its share of L
+    const int pw = p0 + my_pl;
+    float w = 0.f;
+    if (pw < P) {
+      const float mv = __ldg(mp.a.ms[pw] + my_si);
+      w = (mv == -INFINITY) ? 0.f : exp2f(mv - Mx);
+      Lsum = fmaf(__ldg(mp.a.ls[pw] + my_si), w, Lsum);
     }
-    if (pi + 1 < mp.a.P) {
-      mlv = mln;
+    const int pend = min(P, p0 + PC);
+    for (int p = p0; p < pend; ++p) {
+      float on[R][V];
+      if (p + 1 < P) load(p + 1, on);
 #pragma unroll
-      for (int r = 0; r < R; ++r)
+      for (int r = 0; r < R; ++r) {
+        const float wr = __shfl_sync(0xffffffffu, w, (p - p0) * R + r);
 #pragma unroll
-        for (int i = 0; i < V; ++i) ov[r][i] = on[r][i];
+        for (int i = 0; i < V; ++i) acc[r][i] = fmaf(ov[r][i], wr, acc[r][i]);
+      }
+      if (p + 1 < P) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int i = 0; i < V; ++i) ov[r][i] = on[r][i];
+      }
     }
   }
 #pragma unroll
+  for (int o = R; o < 32; o <<= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+#pragma unroll
   for (int r = 0; r < R; ++r) {
+    const float L = __shfl_sync(0xffffffffu, Lsum, r);
+    const float M = __shfl_sync(0xffffffffu, Mx, r);
     const int hh = __shfl_sync(0xffffffffu, my_h, r);
     const int ss = __shfl_sync(0xffffffffu, my_s, r);
     const int bb = __shfl_sync(0xffffffffu, my_b, r);
     if (r >= nlive) continue;
-    const float inv = (L[r] > 0.f) ? 1.f / L[r] : 0.f;
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
     const int orow = (mp.out_row != nullptr) ? mp.out_row[ss] : ss;
     const long long od = ((static_cast<long long>(bb) * mp.S_out + orow) * mp.Hq + hh) * D + lane * V;
     if (mp.out_dtype == RA_F32) {
@@ -233,17 +245,17 @@ __global__ void __launch_bounds__(256, 3) merge_kernel(const MergeParams mp) {
       if constexpr (V == 4) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(acc[r][0] * inv, acc[r][1] * inv);
         __nv_bfloat162 hi = __floats2bfloat162_rn(acc[r][2] * inv, acc[r][3] * inv);
-        uint2 w;
-        w.x = *reinterpret_cast<uint32_t*>(&lo);
-        w.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(o) = w;
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo);
+        u.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(o) = u;
       } else {
         *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc[r][0] * inv, acc[r][1] * inv);
       }
     }
     if (lane == 0 && mp.lse != nullptr)
       mp.lse[(static_cast<long long>(bb) * mp.Hq + hh) * mp.S_out + orow] =
-          (L[r] > 0.f) ? (M[r] + log2f(L[r])) * 0.69314718055994531f : -INFINITY;
+          (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
 }
 
