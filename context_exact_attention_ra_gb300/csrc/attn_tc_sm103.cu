@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const Abort ab{abort_flag, p.err};
 
-  const int warp = threadIdx.x >> 5;
+  // taken from lane 0 so that the compiler can keep it in a uniform register
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
 
   // ---- which problem this block owns -----------------------------------
