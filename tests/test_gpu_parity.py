@@ -229,9 +229,11 @@ def test_block_attn_arbitrary_positions_and_state(dtype):
     assert int(work[0].item()) == pairs * B * Hq
 
 
-@pytest.mark.parametrize("P", [1, 3])
-def test_lse_merge_of_key_splits_equals_full_attention(P):
-    B, S, Hq, Hkv, D = 1, 512, 4, 1, 128
+# P = 9 and 64 take the merge through more than one pass of per-partial weights
+# (eight partials per pass); D = 64 the two-column-per-lane form
+@pytest.mark.parametrize("P,D", [(1, 128), (3, 128), (9, 128), (64, 128), (9, 64)])
+def test_lse_merge_of_key_splits_equals_full_attention(P, D):
+    B, S, Hq, Hkv = 1, 512, 4, 1
     g = torch.Generator().manual_seed(11)
     q = torch.randn((B, S, Hq, D), generator=g).to(torch.bfloat16)
     k = torch.randn((B, S, Hkv, D), generator=g).to(torch.bfloat16)
