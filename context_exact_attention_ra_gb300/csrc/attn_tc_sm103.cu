@@ -732,7 +732,8 @@ int launch_d(const AttnParams& p, const void* q, const void* k, const void* v,
   cudaError_t ce = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (ce != cudaSuccess) return static_cast<int>(ce);
-  dim3 grid(static_cast<unsigned>(p.B * p.Hq), static_cast<unsigned>(p.c * p.q_blocks_per_rank));
+  const int yb = (p.y_blocks > 0) ? p.y_blocks : p.c * p.q_blocks_per_rank;
+  dim3 grid(static_cast<unsigned>(p.B * p.Hq), static_cast<unsigned>(yb));
   launch_stage() = "tensor-core kernel launch";
   attn_fwd_tc_kernel<D><<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
   return static_cast<int>(cudaGetLastError());

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include <nvtx3/nvToolsExt.h>
@@ -704,6 +705,145 @@ void* device_view(void* host) {
 }
 }  // namespace
 
+namespace {
+// Streams and events of the pipelined host-buffer ring, created once per
+// device: a second stream for attention launches, one for the Q copies and a
+// pool of events.  The mutex keeps one call's sequence of records and waits
+// together when several host threads use the same device.
+struct HostioRes {
+  std::mutex mu;
+  cudaStream_t attn2 = nullptr;
+  cudaStream_t copy = nullptr;
+  std::vector<cudaEvent_t> ev;
+};
+
+HostioRes* hostio_res(size_t nev, cudaError_t* ce) {
+  static HostioRes res[64];
+  int dev = 0;
+  *ce = cudaGetDevice(&dev);
+  if (*ce != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *ce = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  HostioRes* r = &res[dev];
+  if (r->attn2 == nullptr) {
+    *ce = cudaStreamCreateWithFlags(&r->attn2, cudaStreamNonBlocking);
+    if (*ce == cudaSuccess) *ce = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
+    if (*ce != cudaSuccess) return nullptr;
+  }
+  while (r->ev.size() < nev) {
+    cudaEvent_t e;
+    *ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (*ce != cudaSuccess) return nullptr;
+    r->ev.push_back(e);
+  }
+  return r;
+}
+
+// The fused ring with host inputs and outputs, pipelined: K, V and the
+// positions are packed first (read over the CPU-GPU link by the pack kernel,
+// or copied first when not mapped); each rank's query rows, which are one or
+// two contiguous stretches of the natural order per batch in the contiguous
+// and zig-zag layouts, are copied by the copy engine on a stream of their own;
+// each rank's query blocks then run as a launch of their own, in heavy-first
+// order within the rank, as soon as that rank's rows have landed.  Launches
+// alternate between the caller's stream and a second one, so that one
+// launch's last blocks overlap the next one's first.  The kernels write the
+// mapped outputs directly.
+ra_status hostio_pipelined(const void* q_host, const void* k_src, const void* v_src, ra_shape shp,
+                           int c, int layout, int causal, int out_dtype, void* out_dst, float* lse_dst,
+                           void* workspace, cudaStream_t s) {
+  const RingWs w = ring_ws(shp, c, RA_MODE_FUSED);
+  const int S = shp.Sq;
+  const int n = S / c;
+  const int bpr = blocks_per_rank(shp, n);
+  cudaError_t ce = cudaSuccess;
+  HostioRes* res = hostio_res(static_cast<size_t>(c) + 3, &ce);
+  if (res == nullptr) return cuda_fail(ce, "stream / event creation");
+  std::lock_guard<std::mutex> lock(res->mu);
+  cudaEvent_t e_entry = res->ev[0], e_prep = res->ev[1], e_done2 = res->ev[2];
+  char* qp = at<char>(workspace, w.qp);
+  const char* qh = static_cast<const char*>(q_host);
+  const size_t row_bytes = static_cast<size_t>(shp.Hq) * shp.D * elem_bytes(shp.dtype);
+
+  // Q: rank by rank on the copy stream
+  ce = cudaEventRecord(e_entry, s);
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(res->copy, e_entry, 0);
+  for (int r = 0; r < c && ce == cudaSuccess; ++r) {
+    for (int b = 0; b < shp.B && ce == cudaSuccess; ++b) {
+      const size_t brow = static_cast<size_t>(b) * S;
+      if (layout == RA_ZIGZAG) {
+        const int ch = n / 2;
+        ce = cudaMemcpyAsync(qp + (brow + static_cast<size_t>(r) * n) * row_bytes,
+                             qh + (brow + static_cast<size_t>(r) * ch) * row_bytes,
+                             static_cast<size_t>(ch) * row_bytes, cudaMemcpyHostToDevice, res->copy);
+        if (ce == cudaSuccess)
+          ce = cudaMemcpyAsync(qp + (brow + static_cast<size_t>(r) * n + ch) * row_bytes,
+                               qh + (brow + static_cast<size_t>(2 * c - 1 - r) * ch) * row_bytes,
+                               static_cast<size_t>(ch) * row_bytes, cudaMemcpyHostToDevice, res->copy);
+      } else {
+        ce = cudaMemcpyAsync(qp + (brow + static_cast<size_t>(r) * n) * row_bytes,
+                             qh + (brow + static_cast<size_t>(r) * n) * row_bytes,
+                             static_cast<size_t>(n) * row_bytes, cudaMemcpyHostToDevice, res->copy);
+      }
+    }
+    if (ce == cudaSuccess) ce = cudaEventRecord(res->ev[3 + r], res->copy);
+  }
+  if (ce != cudaSuccess) return cuda_fail(ce, "Q copies");
+
+  // K, V, positions, tile ranges and the per-rank block order on the caller's stream
+  int e = ra::launch_pack(nullptr, k_src, v_src, shp.B, S, shp.Hq, shp.Hkv, shp.D, elem_bytes(shp.dtype),
+                          c, layout, qp, at<void>(workspace, w.kp), at<void>(workspace, w.vp),
+                          at<int32_t>(workspace, w.pos), s);
+  if (!e) e = ra::launch_tile_ranges(at<int32_t>(workspace, w.pos), c, n, at<int2>(workspace, w.ranges), s);
+  if (!e)
+    e = ra::launch_block_order(at<int32_t>(workspace, w.pos), c, n, rows_per_block(shp.dtype), bpr,
+                               at<int32_t>(workspace, w.order), s, 1);
+  if (e) return cuda_fail(e, ra::launch_stage());
+  ce = cudaEventRecord(e_prep, s);
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(res->attn2, e_prep, 0);
+  if (ce != cudaSuccess) return cuda_fail(ce, "event (prepare)");
+
+  int err = 0;
+  unsigned int* ew = ra::device_error_word(&err);
+  if (ew == nullptr) return cuda_fail(err, "device error word lookup");
+  AttnParams p = base_params(shp, c, n, n, causal);
+  p.k_sorted = 1;
+  p.q_pos = at<int32_t>(workspace, w.pos);
+  p.k_pos = p.q_pos;
+  p.k_ranges = at<int2>(workspace, w.ranges);
+  p.q = qp;
+  p.k = at<void>(workspace, w.kp);
+  p.v = at<void>(workspace, w.vp);
+  p.err = ew;
+  p.out = out_dst;
+  p.out_f32 = (out_dtype == RA_F32) ? 1 : 0;
+  p.lse = lse_dst;
+  p.S_out = S;
+  p.t_begin = 0;
+  p.t_end = c;
+  p.finalize = 1;
+  p.y_blocks = bpr;
+  ra_status st = RA_OK;
+  for (int r = 0; r < c && st == RA_OK; ++r) {
+    cudaStream_t sr = (r & 1) ? res->attn2 : s;
+    ce = cudaStreamWaitEvent(sr, res->ev[3 + r], 0);
+    if (ce != cudaSuccess) {
+      st = cuda_fail(ce, "event (Q rows)");
+      break;
+    }
+    p.block_order = at<int32_t>(workspace, w.order) + static_cast<size_t>(r) * bpr;
+    st = launch_attn(p, shp, S, S, sr);
+  }
+  // join the second stream back into the caller's, also after an error
+  ce = cudaEventRecord(e_done2, res->attn2);
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, e_done2, 0);
+  if (st == RA_OK && ce != cudaSuccess) st = cuda_fail(ce, "event (join)");
+  return st;
+}
+}  // namespace
+
 ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const void* v_host,
                                  ra_shape shp, int c, int layout, int causal, int mode,
                                  int out_dtype, void* out_host, float* lse_host, void* workspace,
@@ -743,6 +883,28 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
   const void* k_src = device_view(const_cast<void*>(k_host));
   const void* v_src = device_view(const_cast<void*>(v_host));
   cudaError_t ce = cudaSuccess;
+  const int n = static_cast<int>(S) / c;
+  const bool pipelined = mode == RA_MODE_FUSED && shp.dtype == RA_BF16 && q_src != nullptr &&
+                         out_dst != dout && (layout == RA_CONTIGUOUS || layout == RA_ZIGZAG) &&
+                         c * blocks_per_rank(shp, n) <= ra::kMaxOrderedBlocks;
+  if (pipelined) {
+    if (k_src == nullptr) {
+      ce = cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s);
+      k_src = dk;
+    }
+    if (ce == cudaSuccess && v_src == nullptr) {
+      ce = cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s);
+      v_src = dv;
+    }
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemcpyAsync (inputs)");
+    st = hostio_pipelined(q_host, k_src, v_src, shp, c, layout, causal, out_dtype, out_dst, lse_dst,
+                          workspace, s);
+    if (st != RA_OK) return st;
+    if (lse_host && lse_dst == dlse) ce = cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, s);
+    if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamSynchronize");
+    return RA_OK;
+  }
   if (q_src == nullptr) {
     ce = cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s);
     q_src = dq;

@@ -59,6 +59,7 @@ struct AttnParams {
   ra_work* work;               // [c*c] (rank*c + step) or nullptr
   unsigned int* err;           // device error word
   const int32_t* block_order;  // [c*q_blocks_per_rank] or nullptr
+  int y_blocks;                // blocks along grid y; 0: c * q_blocks_per_rank (all of them)
 };
 
 // Parameters of the decode (split-K over shards) kernels.
@@ -106,8 +107,10 @@ int launch_pack(const void* q, const void* k, const void* v, int B, int S, int H
                 int D, int elem_bytes, int c, int layout, void* qp, void* kp, void* vp,
                 int32_t* pos, void* stream);
 int launch_tile_ranges(const int32_t* pos, int c, int n, int2* ranges, void* stream);
+// Heavy-first block order; per_rank: each rank's blocks ordered among
+// themselves (rank r's list at order[r * blocks_per_rank]).
 int launch_block_order(const int32_t* pos, int c, int n, int rows_per_block,
-                       int blocks_per_rank, int32_t* order, void* stream);
+                       int blocks_per_rank, int32_t* order, void* stream, int per_rank = 0);
 struct MergeArgs {
   int P;
   const float* outs[RA_MERGE_MAX_PARTIALS];

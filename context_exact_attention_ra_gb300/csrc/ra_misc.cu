@@ -52,9 +52,11 @@ __global__ void pack_kernel(const uint4* q, const uint4* k, const uint4* v, int 
   const int row = blockIdx.x;
   const int b = blockIdx.y;
   const int nat = natural_row(row / n, row % n, n, c, layout);
-  const long long qs = (static_cast<long long>(b) * S + nat) * q_vec;
-  const long long qd = (static_cast<long long>(b) * S + row) * q_vec;
-  for (int i = threadIdx.x; i < q_vec; i += blockDim.x) qp[qd + i] = q[qs + i];
+  if (q != nullptr) {   // null: K, V and positions only (Q is copied separately)
+    const long long qs = (static_cast<long long>(b) * S + nat) * q_vec;
+    const long long qd = (static_cast<long long>(b) * S + row) * q_vec;
+    for (int i = threadIdx.x; i < q_vec; i += blockDim.x) qp[qd + i] = q[qs + i];
+  }
   const long long ks = (static_cast<long long>(b) * S + nat) * kv_vec;
   const long long kd = (static_cast<long long>(b) * S + row) * kv_vec;
   for (int i = threadIdx.x; i < kv_vec; i += blockDim.x) {
@@ -66,33 +68,39 @@ __global__ void pack_kernel(const uint4* q, const uint4* k, const uint4* v, int 
 
 // Heavy-first order of the query blocks of a causal ring: a block's key is
 // the largest position among its rows; blocks are listed by key, descending
-// (ties by index), so the longest causal rows start first.  One thread block;
-// keys live in shared memory.
+// (ties by index), so the longest causal rows start first.  With per_rank the
+// blocks of each rank are ordered among themselves, rank r's list at
+// order[r * blocks_per_rank ...].  One thread block: each warp reduces the
+// keys of a share of the blocks (lanes over rows), keys live in shared memory.
 __global__ void block_order_kernel(const int32_t* pos, int c, int n, int rows_per_block,
-                                   int blocks_per_rank, int32_t* order) {
+                                   int blocks_per_rank, int per_rank, int32_t* order) {
   extern __shared__ int keys[];
   const int total = c * blocks_per_rank;
-  for (int y = threadIdx.x; y < total; y += blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  for (int y = threadIdx.x >> 5; y < total; y += blockDim.x >> 5) {
     const int r = y / blocks_per_rank;
     const int i0 = (y % blocks_per_rank) * rows_per_block;
     const int i1 = min(n, i0 + rows_per_block);
     int mx = INT_MIN;
-    for (int i = i0; i < i1; ++i) mx = max(mx, pos[static_cast<long long>(r) * n + i]);
-    keys[y] = mx;
+    for (int i = i0 + lane; i < i1; i += 32) mx = max(mx, pos[static_cast<long long>(r) * n + i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) keys[y] = mx;
   }
   __syncthreads();
   for (int y = threadIdx.x; y < total; y += blockDim.x) {
     const int ky = keys[y];
+    const int o0 = per_rank ? (y / blocks_per_rank) * blocks_per_rank : 0;
+    const int o1 = per_rank ? o0 + blocks_per_rank : total;
     int before = 0;
-    for (int o = 0; o < total; ++o) {
+    for (int o = o0; o < o1; ++o) {
       const int ko = keys[o];
       before += (ko > ky || (ko == ky && o < y)) ? 1 : 0;
     }
-    order[before] = y;
+    order[o0 + before] = y;
   }
 }
 
-// One warp per 128-row tile of each shard: smallest and largest position.
 __global__ void tile_range_kernel(const int32_t* pos, int c, int n, int tiles, int2* out) {
   const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -372,12 +380,12 @@ int launch_tile_ranges(const int32_t* pos, int c, int n, int2* ranges, void* str
 }
 
 int launch_block_order(const int32_t* pos, int c, int n, int rows_per_block, int blocks_per_rank,
-                       int32_t* order, void* stream) {
+                       int32_t* order, void* stream, int per_rank) {
   const int total = c * blocks_per_rank;
   if (total == 0) return 0;
   if (total > kMaxOrderedBlocks) return static_cast<int>(cudaErrorInvalidValue);
   block_order_kernel<<<1, 1024, total * sizeof(int), static_cast<cudaStream_t>(stream)>>>(
-      pos, c, n, rows_per_block, blocks_per_rank, order);
+      pos, c, n, rows_per_block, blocks_per_rank, per_rank, order);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -228,7 +228,13 @@ ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const voi
  * ra_ring_forward_hostio_workspace_size().  When out_host (or lse_host) is
  * pinned memory mapped into the device's address space, the kernels write it
  * directly over the CPU-GPU link while they run; otherwise the result is
- * copied back after the attention. */
+ * copied back after the attention.  The fused bf16 ring with pinned q and a
+ * mapped out in the contiguous or zig-zag layout is pipelined: K, V and the
+ * positions are packed first, each rank's query rows are copied on an
+ * internal copy stream, and each rank's query blocks run as a launch of their
+ * own once those rows have landed, alternating between `stream` and an
+ * internal stream (both joined back into `stream`; the internal streams and
+ * events are created on first use per device and kept). */
 size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode,
                                              int out_dtype);
 ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const void* v_host,
