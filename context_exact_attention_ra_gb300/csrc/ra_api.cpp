@@ -713,7 +713,8 @@ namespace {
 struct HostioRes {
   std::mutex mu;
   cudaStream_t attn2 = nullptr;
-  cudaStream_t copy = nullptr;
+  cudaStream_t copy = nullptr;   // host to device
+  cudaStream_t back = nullptr;   // device to host
   std::vector<cudaEvent_t> ev;
 };
 
@@ -730,6 +731,7 @@ HostioRes* hostio_res(size_t nev, cudaError_t* ce) {
   if (r->attn2 == nullptr) {
     *ce = cudaStreamCreateWithFlags(&r->attn2, cudaStreamNonBlocking);
     if (*ce == cudaSuccess) *ce = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
+    if (*ce == cudaSuccess) *ce = cudaStreamCreateWithFlags(&r->back, cudaStreamNonBlocking);
     if (*ce != cudaSuccess) return nullptr;
   }
   while (r->ev.size() < nev) {
@@ -749,46 +751,57 @@ HostioRes* hostio_res(size_t nev, cudaError_t* ce) {
 // each rank's query blocks then run as a launch of their own, in heavy-first
 // order within the rank, as soon as that rank's rows have landed.  Launches
 // alternate between the caller's stream and a second one, so that one
-// launch's last blocks overlap the next one's first.  The kernels write the
-// mapped outputs directly.
+// launch's last blocks overlap the next one's first.  The output goes to
+// device memory and each rank's rows are copied to out_host on a third stream
+// as soon as its launch has finished (cheaper than the epilogue's stores
+// crossing the link); lse is written where lse_dst points.
 ra_status hostio_pipelined(const void* q_host, const void* k_src, const void* v_src, ra_shape shp,
-                           int c, int layout, int causal, int out_dtype, void* out_dst, float* lse_dst,
-                           void* workspace, cudaStream_t s) {
+                           int c, int layout, int causal, int out_dtype, void* out_host, void* dout,
+                           float* lse_dst, void* workspace, cudaStream_t s) {
   const RingWs w = ring_ws(shp, c, RA_MODE_FUSED);
   const int S = shp.Sq;
   const int n = S / c;
   const int bpr = blocks_per_rank(shp, n);
   cudaError_t ce = cudaSuccess;
-  HostioRes* res = hostio_res(static_cast<size_t>(c) + 3, &ce);
+  HostioRes* res = hostio_res(2 * static_cast<size_t>(c) + 4, &ce);
   if (res == nullptr) return cuda_fail(ce, "stream / event creation");
   std::lock_guard<std::mutex> lock(res->mu);
-  cudaEvent_t e_entry = res->ev[0], e_prep = res->ev[1], e_done2 = res->ev[2];
+  cudaEvent_t e_entry = res->ev[0], e_prep = res->ev[1], e_done2 = res->ev[2], e_back = res->ev[3];
+  cudaEvent_t* e_q = res->ev.data() + 4;       // rank r's query rows landed
+  cudaEvent_t* e_att = res->ev.data() + 4 + c; // rank r's attention finished
   char* qp = at<char>(workspace, w.qp);
   const char* qh = static_cast<const char*>(q_host);
   const size_t row_bytes = static_cast<size_t>(shp.Hq) * shp.D * elem_bytes(shp.dtype);
+  const size_t orow_bytes = static_cast<size_t>(shp.Hq) * shp.D * elem_bytes(out_dtype);
+  // Rank r's rows in the natural order, per batch: one stretch (contiguous)
+  // or two (zig-zag); `to_packed` also gives their place in the rank-major
+  // buffer.  Copies them between dst and src with the given row size.
+  auto copy_rank = [&](int r, char* dst, const char* src, size_t rb, bool to_packed,
+                       cudaMemcpyKind kind, cudaStream_t st) -> cudaError_t {
+    cudaError_t e2 = cudaSuccess;
+    for (int b = 0; b < shp.B && e2 == cudaSuccess; ++b) {
+      const size_t brow = static_cast<size_t>(b) * S;
+      const int parts = (layout == RA_ZIGZAG) ? 2 : 1;
+      const size_t len = static_cast<size_t>(n / parts);
+      for (int part = 0; part < parts && e2 == cudaSuccess; ++part) {
+        const size_t nat = (layout == RA_ZIGZAG) ? static_cast<size_t>(part == 0 ? r : 2 * c - 1 - r) * len
+                                                 : static_cast<size_t>(r) * n;
+        const size_t pk = static_cast<size_t>(r) * n + part * len;
+        const size_t d_row = brow + (to_packed ? pk : nat);
+        const size_t s_row = brow + nat;
+        e2 = cudaMemcpyAsync(dst + d_row * rb, src + s_row * rb, len * rb, kind, st);
+      }
+    }
+    return e2;
+  };
 
   // Q: rank by rank on the copy stream
   ce = cudaEventRecord(e_entry, s);
   if (ce == cudaSuccess) ce = cudaStreamWaitEvent(res->copy, e_entry, 0);
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(res->back, e_entry, 0);
   for (int r = 0; r < c && ce == cudaSuccess; ++r) {
-    for (int b = 0; b < shp.B && ce == cudaSuccess; ++b) {
-      const size_t brow = static_cast<size_t>(b) * S;
-      if (layout == RA_ZIGZAG) {
-        const int ch = n / 2;
-        ce = cudaMemcpyAsync(qp + (brow + static_cast<size_t>(r) * n) * row_bytes,
-                             qh + (brow + static_cast<size_t>(r) * ch) * row_bytes,
-                             static_cast<size_t>(ch) * row_bytes, cudaMemcpyHostToDevice, res->copy);
-        if (ce == cudaSuccess)
-          ce = cudaMemcpyAsync(qp + (brow + static_cast<size_t>(r) * n + ch) * row_bytes,
-                               qh + (brow + static_cast<size_t>(2 * c - 1 - r) * ch) * row_bytes,
-                               static_cast<size_t>(ch) * row_bytes, cudaMemcpyHostToDevice, res->copy);
-      } else {
-        ce = cudaMemcpyAsync(qp + (brow + static_cast<size_t>(r) * n) * row_bytes,
-                             qh + (brow + static_cast<size_t>(r) * n) * row_bytes,
-                             static_cast<size_t>(n) * row_bytes, cudaMemcpyHostToDevice, res->copy);
-      }
-    }
-    if (ce == cudaSuccess) ce = cudaEventRecord(res->ev[3 + r], res->copy);
+    ce = copy_rank(r, qp, qh, row_bytes, true, cudaMemcpyHostToDevice, res->copy);
+    if (ce == cudaSuccess) ce = cudaEventRecord(e_q[r], res->copy);
   }
   if (ce != cudaSuccess) return cuda_fail(ce, "Q copies");
 
@@ -817,7 +830,7 @@ ra_status hostio_pipelined(const void* q_host, const void* k_src, const void* v_
   p.k = at<void>(workspace, w.kp);
   p.v = at<void>(workspace, w.vp);
   p.err = ew;
-  p.out = out_dst;
+  p.out = dout;
   p.out_f32 = (out_dtype == RA_F32) ? 1 : 0;
   p.lse = lse_dst;
   p.S_out = S;
@@ -828,17 +841,27 @@ ra_status hostio_pipelined(const void* q_host, const void* k_src, const void* v_
   ra_status st = RA_OK;
   for (int r = 0; r < c && st == RA_OK; ++r) {
     cudaStream_t sr = (r & 1) ? res->attn2 : s;
-    ce = cudaStreamWaitEvent(sr, res->ev[3 + r], 0);
+    ce = cudaStreamWaitEvent(sr, e_q[r], 0);
     if (ce != cudaSuccess) {
       st = cuda_fail(ce, "event (Q rows)");
       break;
     }
     p.block_order = at<int32_t>(workspace, w.order) + static_cast<size_t>(r) * bpr;
     st = launch_attn(p, shp, S, S, sr);
+    if (st != RA_OK) break;
+    // rank r's output rows back to the host as soon as its launch is done
+    ce = cudaEventRecord(e_att[r], sr);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(res->back, e_att[r], 0);
+    if (ce == cudaSuccess)
+      ce = copy_rank(r, static_cast<char*>(out_host), static_cast<const char*>(dout), orow_bytes, false,
+                     cudaMemcpyDeviceToHost, res->back);
+    if (ce != cudaSuccess) st = cuda_fail(ce, "output copies");
   }
-  // join the second stream back into the caller's, also after an error
+  // join the other streams back into the caller's, also after an error
   ce = cudaEventRecord(e_done2, res->attn2);
   if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, e_done2, 0);
+  if (ce == cudaSuccess) ce = cudaEventRecord(e_back, res->back);
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, e_back, 0);
   if (st == RA_OK && ce != cudaSuccess) st = cuda_fail(ce, "event (join)");
   return st;
 }
@@ -897,8 +920,8 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
       v_src = dv;
     }
     if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemcpyAsync (inputs)");
-    st = hostio_pipelined(q_host, k_src, v_src, shp, c, layout, causal, out_dtype, out_dst, lse_dst,
-                          workspace, s);
+    st = hostio_pipelined(q_host, k_src, v_src, shp, c, layout, causal, out_dtype, out_host, dout,
+                          lse_dst, workspace, s);
     if (st != RA_OK) return st;
     if (lse_host && lse_dst == dlse) ce = cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, s);
     if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);

@@ -233,8 +233,10 @@ ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const voi
  * positions are packed first, each rank's query rows are copied on an
  * internal copy stream, and each rank's query blocks run as a launch of their
  * own once those rows have landed, alternating between `stream` and an
- * internal stream (both joined back into `stream`; the internal streams and
- * events are created on first use per device and kept). */
+ * internal stream; the output goes to device memory and each rank's rows are
+ * copied to out_host on another internal stream once its launch is done (all
+ * joined back into `stream`; the internal streams and events are created on
+ * first use per device and kept). */
 size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode,
                                              int out_dtype);
 ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const void* v_host,
