@@ -22,7 +22,8 @@
 //   warps 4-7  softmax for Q1
 //   warp 8     TMA loads of Q and the K tiles
 //   warp 9     TMA loads of the V tiles
-//   warp 10    tensor-memory allocation; its lane 0 alone issues tcgen05.mma
+//   warp 10    tensor-memory allocation and the tcgen05.mma issue loop (the
+//              whole warp runs it; one elected lane issues each instruction)
 // Pipelines: K and V each have 2 shared-memory stages; the two query tiles
 // ping-pong so that the tensor core multiplies one tile while the softmax of
 // the other runs.  Tensor memory (512 columns): S0 | S1 | O0 | O1, with P_h
@@ -333,13 +334,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ===================== tensor-core issue ============================
-    // One thread runs this loop: tcgen05.mma issue holds the issuing thread
+    // The whole warp runs this loop with the same values in every lane, so
+    // the descriptors and addresses stay warp-uniform; one elected lane
+    // issues each tcgen05.mma / commit (no branch around the issue), and the
+    // waits are made warp-uniform.  tcgen05.mma issue holds the issuing lane
     // until the tensor core takes the instruction, so everything between two
     // batches is kept short.
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = ptx::idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idPV = ptx::idesc_bf16_f32(128, D, true);
-      bool ok = wait_bar(bar(L::bQ), 0, ab, kErrTimeoutQ);
+      bool ok = __all_sync(0xffffffffu, wait_bar(bar(L::bQ), 0, ab, kErrTimeoutQ));
       bool issued_any = false;
       // Shared-memory descriptors of the first Q tile / K stage / V stage;
       // the others differ only in the 16-byte address field (bits 0-13).
@@ -352,14 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4);
-          ptx::tc_mma_ss(tmem + col_S(hh), qd + o, kd + o, idS, kk > 0 ? 1u : 0u);
+          ptx::tc_mma_ss_elect(tmem + col_S(hh), qd + o, kd + o, idS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_PV = [&](int hh, int vs) {
         const uint64_t vd = dV + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          ptx::tc_mma_ts(tmem + col_O(hh), tmem + col_S(hh) + kk * 8,
+          ptx::tc_mma_ts_elect(tmem + col_O(hh), tmem + col_S(hh) + kk * 8,
                          vd + static_cast<uint64_t>((kk * 16 * 128) >> 4), idPV, 1u);
       };
 
@@ -381,34 +385,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (k.skip) continue;
           const int ks = static_cast<int>(j % L::KST);
-          ok = wait_bar(bar(L::bKFull + ks), (j / L::KST) & 1u, ab, kErrTimeoutK);
+          ok = __all_sync(0xffffffffu, wait_bar(bar(L::bKFull + ks), (j / L::KST) & 1u, ab, kErrTimeoutK));
           if (!ok) break;
           ptx::tc_fence_after_sync();
           if (j == 0) {
             for (int hh = 0; hh < 2; ++hh) {
               issue_S(hh, ks);
-              ptx::tc_commit(bar(L::bSFull + hh));
+              ptx::tc_commit_elect(bar(L::bSFull + hh));
             }
             issued_any = true;
           } else {
             const uint32_t jp = j - 1;
             const int vs = static_cast<int>(jp % L::VST);
-            ok = wait_bar(bar(L::bVFull + vs), (jp / L::VST) & 1u, ab, kErrTimeoutV);
+            ok = __all_sync(0xffffffffu, wait_bar(bar(L::bVFull + vs), (jp / L::VST) & 1u, ab, kErrTimeoutV));
             for (int hh = 0; hh < 2 && ok; ++hh) {
-              ok = wait_bar(bar(L::bPFull + hh), jp & 1u, ab, kErrTimeoutP);
+              ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPFull + hh), jp & 1u, ab, kErrTimeoutP));
               if (!ok) break;
               ptx::tc_fence_after_sync();
               issue_PV(hh, vs);
               issue_S(hh, ks);
-              ptx::tc_commit(bar(L::bSFull + hh));
+              ptx::tc_commit_elect(bar(L::bSFull + hh));
             }
-            if (ok) ptx::tc_commit(bar(L::bVEmpty + vs));
+            if (ok) ptx::tc_commit_elect(bar(L::bVEmpty + vs));
           }
           if (!ok) break;
-          ptx::tc_commit(bar(L::bKEmpty + ks));
+          ptx::tc_commit_elect(bar(L::bKEmpty + ks));
           ++j;
         }
-        if (p.work != nullptr && ok) {
+        if (p.work != nullptr && ok && lane == 0) {
           ra_work* w = p.work + static_cast<long long>(rank) * p.c + t;
           atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_full), nfull);
           atomicAdd(reinterpret_cast<unsigned long long*>(&w->tiles_partial), npart);
@@ -418,18 +422,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && j > 0) {
         const uint32_t jp = j - 1;
         const int vs = static_cast<int>(jp % L::VST);
-        ok = wait_bar(bar(L::bVFull + vs), (jp / L::VST) & 1u, ab, kErrTimeoutV);
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bVFull + vs), (jp / L::VST) & 1u, ab, kErrTimeoutV));
         for (int hh = 0; hh < 2 && ok; ++hh) {
-          ok = wait_bar(bar(L::bPFull + hh), jp & 1u, ab, kErrTimeoutP);
+          ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPFull + hh), jp & 1u, ab, kErrTimeoutP));
           if (!ok) break;
           ptx::tc_fence_after_sync();
           issue_PV(hh, vs);
         }
-        if (ok) ptx::tc_commit(bar(L::bOFinal));
+        if (ok) ptx::tc_commit_elect(bar(L::bOFinal));
       }
       if (!ok && issued_any) {
         // Drain the tensor core before tensor memory is released.
-        ptx::tc_commit(bar(L::bDrain));
+        ptx::tc_commit_elect(bar(L::bDrain));
         if (!wait_bar_drain(bar(L::bDrain), 0)) atomicOr(p.err, kErrTimeoutDrain);
       }
     }
