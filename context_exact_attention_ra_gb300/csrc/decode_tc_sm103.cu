@@ -23,7 +23,9 @@
 // the epilogue.  Every thread also owns one output column of O^T and rescales it
 // when a row's maximum rose.  K and V tiles stream through three shared-memory
 // stages by TMA, so the block reads each key and value byte once, and the
-// kernel is bound by HBM bandwidth.
+// kernel is bound by HBM bandwidth; the loads carry an evict-first L2 policy,
+// so that the stream displaces its own lines rather than whatever else L2
+// holds (often lines that would first have to be written back).
 //
 // Warp roles (192 threads): warps 0-3 softmax and epilogue, warp 4 TMA loads,
 // warp 5 tensor-memory allocation; its lane 0 issues the MMAs.  Every wait is
@@ -235,6 +237,8 @@ __global__ void __launch_bounds__(kDTThreads, 1)
   if (warp == kDTWarpLoad) {
     // ===================== TMA loads of the K and V tiles =================
     if (lane == 0) {
+      // every K and V byte is read once: its lines go first when L2 needs room
+      const uint64_t pol = ptx::l2_policy_evict_first();
       int issued = 0;
       bool ok = !*abort_flag;
       for (int j = 0; j < J && ok; ++j) {
@@ -246,10 +250,10 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         const int nat0 = static_cast<int>(dt_natural_key(shard, lt * kDTKeys, p.n, p.c, p.layout));
         ptx::mbar_arrive_expect_tx(bar(L::bKVFull + st), 2 * L::kKVTile);
         for (int x = 0; x < 2; ++x) {
-          ptx::tma_load_4d(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
-                           x * L::kBox, g, nat0, b);
-          ptx::tma_load_4d(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
-                           x * L::kBox, g, nat0, b);
+          ptx::tma_load_4d_hint(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
+                                x * L::kBox, g, nat0, b, pol);
+          ptx::tma_load_4d_hint(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
+                                x * L::kBox, g, nat0, b, pol);
         }
         ++issued;
       }
