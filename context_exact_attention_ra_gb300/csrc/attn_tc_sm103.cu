@@ -292,11 +292,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage0 = sbase + (is_k ? L::kK : L::kV);
     const bool q_issued = is_k && !*abort_flag;
     if (q_issued && lane == 0) {
+      // Q tiles are read by this block only: their lines go first when L2
+      // needs room, which keeps the key and value tiles (read by every
+      // block) resident
+      const uint64_t pol = ptx::l2_policy_evict_first();
       ptx::mbar_arrive_expect_tx(bar(L::bQ), 2 * L::kTileBytes);
       for (int hh = 0; hh < 2; ++hh)
         for (int x = 0; x < L::kBoxes; ++x)
-          ptx::tma_load_4d(sbase + L::kQ + hh * L::kTileBytes + x * L::kBoxBytes, &tm_q,
-                           bar(L::bQ), x * L::kBox, h, rank * p.n_q + row0 + hh * kTile, b);
+          ptx::tma_load_4d_hint(sbase + L::kQ + hh * L::kTileBytes + x * L::kBoxBytes, &tm_q,
+                                bar(L::bQ), x * L::kBox, h, rank * p.n_q + row0 + hh * kTile, b, pol);
     }
     uint32_t j = 0;
     bool ok = !*abort_flag;
