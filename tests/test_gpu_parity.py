@@ -262,27 +262,30 @@ def test_lse_merge_of_key_splits_equals_full_attention(P, D):
 # The fused ring with pinned queries and outputs in the contiguous or zig-zag
 # layout runs pipelined (K and V packed first, each rank's query rows copied and
 # its blocks launched on their own); the other cases go through one launch.
-@pytest.mark.parametrize("mode,pinned_out,layout,B,pinned_kv", [
-    ("fused", True, "zigzag", 1, True),
-    ("fused", False, "zigzag", 1, True),
-    ("per_step", True, "zigzag", 1, True),
-    ("fused", True, "contiguous", 2, True),
-    ("fused", True, "zigzag", 2, False),
-    ("fused", True, "striped", 1, True),
+@pytest.mark.parametrize("mode,pinned_out,layout,B,pinned_kv,out_f32", [
+    ("fused", True, "zigzag", 1, True, False),
+    ("fused", False, "zigzag", 1, True, False),
+    ("per_step", True, "zigzag", 1, True, False),
+    ("fused", True, "contiguous", 2, True, False),
+    ("fused", True, "zigzag", 2, False, False),
+    ("fused", True, "striped", 1, True, False),
+    ("fused", True, "zigzag", 1, True, True),
 ])
-def test_hostio_equals_device_path(mode, pinned_out, layout, B, pinned_kv):
+def test_hostio_equals_device_path(mode, pinned_out, layout, B, pinned_kv, out_f32):
     w = small_case(2048, 4, layout, True, B=B, Hq=4, Hkv=1, D=128, seed=21)
     q, k, v, _ = make_inputs(w)
-    out_d, lse_d = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, layout, True, mode)
+    odt = torch.float32 if out_f32 else None
+    out_d, lse_d = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, layout, True, mode, out_dtype=odt)
     qh = q.pin_memory()
     kh, vh = (k.pin_memory(), v.pin_memory()) if pinned_kv else (k.clone(), v.clone())
-    out_h = torch.empty_like(qh)
+    out_h = torch.empty(q.shape, dtype=torch.float32) if out_f32 else torch.empty_like(qh)
     lse_h = torch.empty((B, w.Hq, w.S), dtype=torch.float32)
     if pinned_out:
         out_h, lse_h = out_h.pin_memory(), lse_h.pin_memory()
+    bits = torch.int32 if out_f32 else torch.int16
     for _ in range(2):   # the second call reuses the internal streams and events
         ra.ring_forward_hostio(qh, kh, vh, w.c, layout, True, mode, out_host=out_h, lse_host=lse_h)
-        assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
+        assert torch.equal(out_h.view(bits), out_d.cpu().view(bits))
         assert torch.equal(lse_h.view(torch.int32), lse_d.cpu().view(torch.int32))
 
 
