@@ -262,17 +262,18 @@ def test_lse_merge_of_key_splits_equals_full_attention(P, D):
 # The fused ring with pinned queries and outputs in the contiguous or zig-zag
 # layout runs pipelined (K and V packed first, each rank's query rows copied and
 # its blocks launched on their own); the other cases go through one launch.
-@pytest.mark.parametrize("mode,pinned_out,layout,B,pinned_kv,out_f32", [
-    ("fused", True, "zigzag", 1, True, False),
-    ("fused", False, "zigzag", 1, True, False),
-    ("per_step", True, "zigzag", 1, True, False),
-    ("fused", True, "contiguous", 2, True, False),
-    ("fused", True, "zigzag", 2, False, False),
-    ("fused", True, "striped", 1, True, False),
-    ("fused", True, "zigzag", 1, True, True),
+@pytest.mark.parametrize("mode,pinned_out,layout,B,pinned_kv,out_f32,S,c", [
+    ("fused", True, "zigzag", 1, True, False, 2048, 4),
+    ("fused", False, "zigzag", 1, True, False, 2048, 4),
+    ("per_step", True, "zigzag", 1, True, False, 2048, 4),
+    ("fused", True, "contiguous", 2, True, False, 2048, 4),
+    ("fused", True, "zigzag", 2, False, False, 2048, 4),
+    ("fused", True, "striped", 1, True, False, 2048, 4),
+    ("fused", True, "zigzag", 1, True, True, 2048, 4),
+    ("fused", True, "zigzag", 1, True, False, 4096, 16),   # 16 launches of one block row each
 ])
-def test_hostio_equals_device_path(mode, pinned_out, layout, B, pinned_kv, out_f32):
-    w = small_case(2048, 4, layout, True, B=B, Hq=4, Hkv=1, D=128, seed=21)
+def test_hostio_equals_device_path(mode, pinned_out, layout, B, pinned_kv, out_f32, S, c):
+    w = small_case(S, c, layout, True, B=B, Hq=4, Hkv=1, D=128, seed=21)
     q, k, v, _ = make_inputs(w)
     odt = torch.float32 if out_f32 else None
     out_d, lse_d = ra.ring_forward(q.to(DEV), k.to(DEV), v.to(DEV), w.c, layout, True, mode, out_dtype=odt)
