@@ -140,3 +140,39 @@ def test_expected_work_at_c16_reproduces_the_plate():
 def test_selftest_rejects_a_bad_limit_before_any_launch(lib):
     assert lib.ra_selftest_wait_timeout(ctypes.c_uint32(0), ctypes.c_void_p(0)) == -1
     assert lib.ra_selftest_wait_timeout(ctypes.c_uint32(2000000), ctypes.c_void_p(0)) == -1
+
+
+def test_other_entry_points_reject_bad_arguments_before_launch(lib):
+    """Host-buffer ring, decode and rotating ring: every argument error is
+    caught on the host before any CUDA call (these run without a GPU)."""
+    shp = _shape()
+    ok = ctypes.c_void_p(0x100000)   # aligned, never dereferenced on these paths
+    # host-buffer ring
+    hio = lib.ra_ring_forward_hostio
+    assert hio(None, None, None, _shape(S=250), 4, ra.ZIGZAG, 1, 0, ra.BF16, None, None, None, 0, None) == -1
+    assert hio(None, None, None, shp, 2, ra.ZIGZAG, 1, 9, ra.BF16, None, None, None, 0, None) == -1   # mode
+    assert hio(None, None, None, shp, 2, ra.ZIGZAG, 1, 0, 7, None, None, None, 0, None) == -1         # out dtype
+    assert hio(None, None, None, shp, 2, ra.ZIGZAG, 1, 0, ra.BF16, None, None, None, 0, None) == -1   # null
+    assert hio(ok, ok, ok, shp, 2, ra.ZIGZAG, 1, 0, ra.BF16, ok, None, None, 0, None) == -5           # workspace
+    assert hio(None, None, None, _shape(S=0), 2, ra.ZIGZAG, 1, 0, ra.BF16, None, None, None, 0, None) == 0
+    assert lib.ra_ring_forward_hostio_workspace_size(_shape(S=250), 4, ra.ZIGZAG, 0, ra.BF16) == 0
+    assert (lib.ra_ring_forward_hostio_workspace_size(shp, 2, ra.ZIGZAG, 0, ra.BF16) >
+            lib.ra_ring_forward_workspace_size(shp, 2, ra.ZIGZAG, 0))
+    # decode: R = 1 new token over S = 256 keys
+    dec = lib.ra_decode_forward
+    dshp = ra.Shape(1, 1, 256, 4, 2, 128, ra.BF16, 0.088)
+    bad_s = ra.Shape(1, 1, 250, 4, 2, 128, ra.BF16, 0.088)
+    f32 = ra.Shape(1, 1, 256, 4, 2, 128, ra.F32, 0.088)
+    assert dec(None, None, None, None, bad_s, 4, ra.ZIGZAG, 1, ra.BF16, None, None, None, 0, None) == -1
+    assert dec(None, None, None, None, f32, 2, ra.ZIGZAG, 1, ra.BF16, None, None, None, 0, None) == -2
+    assert dec(None, None, None, None, dshp, 2, ra.ZIGZAG, 1, 7, None, None, None, 0, None) == -1
+    assert dec(None, None, None, None, dshp, 2, ra.ZIGZAG, 1, ra.BF16, None, None, None, 0, None) == -1
+    assert dec(ok, ok, ok, ok, dshp, 2, ra.ZIGZAG, 1, ra.BF16, ok, None, None, 0, None) == -5
+    assert lib.ra_decode_workspace_size(bad_s, 4, ra.ZIGZAG) == 0
+    assert lib.ra_decode_workspace_size(dshp, 2, ra.ZIGZAG) > 0
+    # rotating ring: overlap needs a copy stream of its own
+    rot = lib.ra_ring_forward_rotate
+    assert rot(None, None, None, _shape(S=250), 4, ra.ZIGZAG, 1, 0, ra.BF16, None, None, None, 0, None, None) == -1
+    assert rot(None, None, None, shp, 2, ra.ZIGZAG, 1, 1, ra.BF16, None, None, None, 0, None, None) == -1
+    assert rot(None, None, None, shp, 2, ra.ZIGZAG, 1, 0, ra.BF16, None, None, None, 0, None, None) == -1
+    assert rot(ok, ok, ok, shp, 2, ra.ZIGZAG, 1, 0, ra.BF16, ok, None, None, 0, None, None) == -5
