@@ -101,7 +101,7 @@ _SIGS = {
     "ra_work_expected": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(Work)]),
     "ra_device_error": (ctypes.c_int, [_P]),
-    "ra_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
+    "ra_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, ctypes.c_int, _P]),
     "ra_ring_forward_noalloc": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
 }
@@ -180,22 +180,26 @@ def _out_code(out_dtype, q):
 
 
 def ring_forward(q, k, v, c, layout="zigzag", causal=True, mode="fused", scale=None,
-                 workspace=None, report=False, stream=None, out_dtype=None):
+                 workspace=None, report=False, stream=None, out_dtype=None, out=None, lse=None):
     """Ring attention of q [B,S,Hq,D] over k, v [B,S,Hkv,D] with c virtual ranks.
 
     Returns (out [B,S,Hq,D] in out_dtype (default q's dtype; torch.float32
     gives the result before its rounding to bf16), lse [B,Hq,S] float32) and,
     with ``report=True``, a dict of per-(rank, step) work counted on the GPU,
-    the ring schedule and the derived quantities.
+    the ring schedule and the derived quantities.  ``out`` and ``lse`` may be
+    given (contiguous, of those shapes; out's dtype then sets out_dtype).
     """
     _contig(q, k, v)
     lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     md = MODES[mode] if isinstance(mode, str) else int(mode)
     scale = q.shape[-1] ** -0.5 if scale is None else scale
     shp = _shape(q, k, scale)
-    ocode, odt = _out_code(out_dtype, q)
-    out = torch.empty(q.shape, dtype=odt, device=q.device)
-    lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
+    ocode, odt = _out_code(out.dtype if out is not None else out_dtype, q)
+    if out is None:
+        out = torch.empty(q.shape, dtype=odt, device=q.device)
+    if lse is None:
+        lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
+    _contig(out, lse)
     need = ring_workspace_size(shp, c, lay, md)
     if need == 0 and q.numel() > 0:
         raise RaError(-1, "ra_ring_forward_workspace_size")
@@ -431,7 +435,10 @@ def device_error(stream=None):
     _check(lib().ra_device_error(_stream(stream)), "device wait")
 
 
-def selftest_wait_timeout(limit_us=20000, stream=None):
+def selftest_wait_timeout(limit_us=20000, stream=None, leave_pending=False):
     """Run the device-timeout self-test: a bounded wait on a barrier that
-    nothing arrives on.  Returns the status (TIMEOUT when the path works)."""
-    return int(lib().ra_selftest_wait_timeout(int(limit_us), _stream(stream)))
+    nothing arrives on.  Returns the status (TIMEOUT when the path works).
+    With leave_pending the error stays set, as after a real timeout, until
+    device_error() reads and clears it."""
+    return int(lib().ra_selftest_wait_timeout(int(limit_us), 1 if leave_pending else 0,
+                                              _stream(stream)))

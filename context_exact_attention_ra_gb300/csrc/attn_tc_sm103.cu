@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && issued_any) {
         // Drain the tensor core before tensor memory is released.
         ptx::tc_commit_elect(bar(L::bDrain));
-        if (!wait_bar_drain(bar(L::bDrain), 0)) atomicOr(p.err, kErrTimeoutDrain);
+        if (!wait_bar_drain(bar(L::bDrain), 0)) raise_error(p.err, kErrTimeoutDrain);
       }
     }
     __syncwarp();

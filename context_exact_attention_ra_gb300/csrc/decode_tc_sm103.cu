@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
       }
       if (!ok && issued_any) {
         ptx::tc_commit(bar(L::bDrain));
-        if (!wait_bar_drain(bar(L::bDrain), 0)) atomicOr(p.err, kErrTimeoutDrain);
+        if (!wait_bar_drain(bar(L::bDrain), 0)) raise_error(p.err, kErrTimeoutDrain);
       }
     }
     __syncwarp();

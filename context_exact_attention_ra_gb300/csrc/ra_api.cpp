@@ -152,6 +152,25 @@ AttnParams base_params(const ra_shape& s, int c, int n_q, int n_k, int causal) {
   return p;
 }
 
+// The device error word of the current device for the kernels.  A bounded
+// wait that ran out earlier on this device, and has not yet been read with
+// ra_device_error(), is seen here through the word's host mirror (a plain
+// host read, no synchronisation) and refuses the call with RA_ERR_TIMEOUT:
+// kernels launched while the word is set would return without computing.
+ra_status error_word_or_refuse(unsigned int** ew) {
+  int err = 0;
+  volatile unsigned int* mirror = nullptr;
+  *ew = ra::device_error_word(&err, &mirror);
+  if (*ew == nullptr) return cuda_fail(err, "device error word lookup");
+  if (mirror != nullptr && *mirror != 0u) {
+    std::snprintf(g_last_error, sizeof(g_last_error),
+                  "a device wait timed out earlier on this device and is still pending; "
+                  "ra_device_error() reads and clears it");
+    return RA_ERR_TIMEOUT;
+  }
+  return RA_OK;
+}
+
 ra_status launch_attn(const AttnParams& p, const ra_shape& s, long long q_rows, long long k_rows,
                       void* stream) {
   if (static_cast<long long>(p.c) * p.q_blocks_per_rank > 65535) return RA_ERR_UNSUPPORTED;
@@ -186,6 +205,9 @@ ra_status ra_state_init(ra_shape shp, float* o, float* m, float* l, ra_stream_t 
   if (st != RA_OK) return st;
   if (shp.B == 0 || shp.Sq == 0) return RA_OK;
   if (o == nullptr || m == nullptr || l == nullptr || !aligned16(o)) return RA_ERR_INVALID;
+  unsigned int* ew = nullptr;
+  st = error_word_or_refuse(&ew);
+  if (st != RA_OK) return st;
   return cuda_status(ra::launch_state_init(shp.B, shp.Sq, shp.Hq, shp.D, o, m, l, stream));
 }
 
@@ -198,9 +220,9 @@ ra_status ra_block_attn(const void* q, const void* k, const void* v, const int32
   if (!q || !k || !v || !q_pos || !k_pos || !o || !m || !l) return RA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RA_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(work) & 7u) != 0) return RA_ERR_INVALID;
-  int err = 0;
-  unsigned int* ew = ra::device_error_word(&err);
-  if (ew == nullptr) return cuda_fail(err, "device error word lookup");
+  unsigned int* ew = nullptr;
+  st = error_word_or_refuse(&ew);
+  if (st != RA_OK) return st;
   AttnParams p = base_params(shp, 1, shp.Sq, shp.Sk, causal);
   p.q_pos = q_pos;
   p.k_pos = k_pos;
@@ -238,6 +260,9 @@ ra_status ra_lse_merge(int P, const float* const* outs, const float* const* ms,
     a.ms[i] = ms[i];
     a.ls[i] = ls[i];
   }
+  unsigned int* ew = nullptr;
+  st = error_word_or_refuse(&ew);
+  if (st != RA_OK) return st;
   return cuda_status(ra::launch_merge(a, shp.B, shp.Sq, shp.Hq, shp.D, shp.dtype, out, lse,
                                       nullptr, shp.Sq, stream));
 }
@@ -259,6 +284,9 @@ ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape 
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       ws_bytes < w.total)
     return RA_ERR_WORKSPACE;
+  unsigned int* ew = nullptr;
+  st = error_word_or_refuse(&ew);
+  if (st != RA_OK) return st;
   int e = ra::launch_pack(q, k, v, shp.B, shp.Sq, shp.Hq, shp.Hkv, shp.D, elem_bytes(shp.dtype),
                           c, layout, at<void>(workspace, w.qp), at<void>(workspace, w.kp),
                           at<void>(workspace, w.vp), at<int32_t>(workspace, w.pos), stream);
@@ -291,9 +319,9 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       ws_bytes < w.total)
     return RA_ERR_WORKSPACE;
-  int err = 0;
-  unsigned int* ew = ra::device_error_word(&err);
-  if (ew == nullptr) return cuda_fail(err, "device error word lookup");
+  unsigned int* ew = nullptr;
+  st = error_word_or_refuse(&ew);
+  if (st != RA_OK) return st;
 
   const int S = shp.Sq;
   const int n = S / c;
@@ -382,7 +410,7 @@ ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const voi
   return RA_OK;
 }
 
-ra_status ra_selftest_wait_timeout(uint32_t limit_us, ra_stream_t stream) {
+ra_status ra_selftest_wait_timeout(uint32_t limit_us, int leave_pending, ra_stream_t stream) {
   if (limit_us == 0 || limit_us > 1000000u) return RA_ERR_INVALID;
   int err = 0;
   unsigned int* ew = ra::device_error_word(&err);
@@ -392,7 +420,12 @@ ra_status ra_selftest_wait_timeout(uint32_t limit_us, ra_stream_t stream) {
   if (e) return cuda_fail(e, "device error word read");
   e = ra::launch_selftest_timeout(ew, static_cast<uint64_t>(limit_us) * 1000u, stream);
   if (e) return cuda_fail(e, ra::launch_stage());
-  return ra_device_error(stream);
+  if (!leave_pending) return ra_device_error(stream);
+  unsigned int v = 0;
+  e = ra::read_and_clear_error(stream, &v, false);
+  if (e) return cuda_fail(e, "device error word read");
+  if (v) std::snprintf(g_last_error, sizeof(g_last_error), "device wait timed out (error bits 0x%x)", v);
+  return v ? RA_ERR_TIMEOUT : RA_OK;
 }
 
 ra_status ra_device_error(ra_stream_t stream) {
@@ -563,9 +596,8 @@ ra_status ra_decode_forward(const void* q, const int32_t* q_pos, const void* k, 
   p.out = out;
   p.out_f32 = out_dtype == RA_F32 ? 1 : 0;
   p.lse = lse;
-  int err = 0;
-  p.err = ra::device_error_word(&err);
-  if (p.err == nullptr) return cuda_fail(err, "device error word lookup");
+  st = error_word_or_refuse(&p.err);
+  if (st != RA_OK) return st;
   return cuda_status(ra::launch_decode(p, stream));
 }
 
@@ -591,9 +623,9 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       ws_bytes < need)
     return RA_ERR_WORKSPACE;
-  int err = 0;
-  unsigned int* ew = ra::device_error_word(&err);
-  if (ew == nullptr) return cuda_fail(err, "device error word lookup");
+  unsigned int* ew = nullptr;
+  st = error_word_or_refuse(&ew);
+  if (st != RA_OK) return st;
   st = ra_ring_prepare(q, k, v, shp, c, layout, workspace, ws_bytes, stream);
   if (st != RA_OK) return st;
 
@@ -707,18 +739,24 @@ void* device_view(void* host) {
 
 namespace {
 // Streams and events of the pipelined host-buffer ring, created once per
-// device: a second stream for attention launches, one for the Q copies and a
-// pool of events.  The mutex keeps one call's sequence of records and waits
-// together when several host threads use the same device.
+// device (per CUDA context: a device reset ends the context and its streams,
+// and the next call creates new ones): a second stream for attention launches,
+// one for the Q copies, one for the output copies and a pool of events.  A
+// call holds the device's mutex from before the streams are created or the
+// pool grows until its last record and wait are enqueued, so host threads that
+// share a device take turns, and no thread's event handles move under it.
 struct HostioRes {
   std::mutex mu;
+  unsigned long long ctx = 0;
   cudaStream_t attn2 = nullptr;
   cudaStream_t copy = nullptr;   // host to device
   cudaStream_t back = nullptr;   // device to host
   std::vector<cudaEvent_t> ev;
 };
 
-HostioRes* hostio_res(size_t nev, cudaError_t* ce) {
+// The device's resources; the caller locks r->mu and then calls
+// hostio_ready(r, nev) before using them.
+HostioRes* hostio_res(cudaError_t* ce) {
   static HostioRes res[64];
   int dev = 0;
   *ce = cudaGetDevice(&dev);
@@ -727,20 +765,33 @@ HostioRes* hostio_res(size_t nev, cudaError_t* ce) {
     *ce = cudaErrorInvalidDevice;
     return nullptr;
   }
-  HostioRes* r = &res[dev];
-  if (r->attn2 == nullptr) {
-    *ce = cudaStreamCreateWithFlags(&r->attn2, cudaStreamNonBlocking);
-    if (*ce == cudaSuccess) *ce = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
-    if (*ce == cudaSuccess) *ce = cudaStreamCreateWithFlags(&r->back, cudaStreamNonBlocking);
-    if (*ce != cudaSuccess) return nullptr;
+  return &res[dev];
+}
+
+// Creates the streams (first use in this context) and grows the event pool
+// to nev; call with r->mu held.
+cudaError_t hostio_ready(HostioRes* r, size_t nev) {
+  const unsigned long long ctx = ra::current_context_id();
+  if (r->attn2 == nullptr || r->ctx != ctx) {
+    // handles of an ended context are not destroyed: they died with it
+    r->attn2 = r->copy = r->back = nullptr;
+    r->ev.clear();
+    cudaError_t ce = cudaStreamCreateWithFlags(&r->attn2, cudaStreamNonBlocking);
+    if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
+    if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&r->back, cudaStreamNonBlocking);
+    if (ce != cudaSuccess) {
+      r->attn2 = nullptr;
+      return ce;
+    }
+    r->ctx = ra::current_context_id();
   }
   while (r->ev.size() < nev) {
     cudaEvent_t e;
-    *ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
-    if (*ce != cudaSuccess) return nullptr;
+    cudaError_t ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (ce != cudaSuccess) return ce;
     r->ev.push_back(e);
   }
-  return r;
+  return cudaSuccess;
 }
 
 // The fused ring with host inputs and outputs, pipelined: K, V and the
@@ -763,9 +814,11 @@ ra_status hostio_pipelined(const void* q_host, const void* k_src, const void* v_
   const int n = S / c;
   const int bpr = blocks_per_rank(shp, n);
   cudaError_t ce = cudaSuccess;
-  HostioRes* res = hostio_res(2 * static_cast<size_t>(c) + 4, &ce);
-  if (res == nullptr) return cuda_fail(ce, "stream / event creation");
+  HostioRes* res = hostio_res(&ce);
+  if (res == nullptr) return cuda_fail(ce, "device lookup");
   std::lock_guard<std::mutex> lock(res->mu);
+  ce = hostio_ready(res, 2 * static_cast<size_t>(c) + 4);
+  if (ce != cudaSuccess) return cuda_fail(ce, "stream / event creation");
   cudaEvent_t e_entry = res->ev[0], e_prep = res->ev[1], e_done2 = res->ev[2], e_back = res->ev[3];
   cudaEvent_t* e_q = res->ev.data() + 4;       // rank r's query rows landed
   cudaEvent_t* e_att = res->ev.data() + 4 + c; // rank r's attention finished
@@ -881,6 +934,9 @@ ra_status ra_ring_forward_hostio(const void* q_host, const void* k_host, const v
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       ws_bytes < need)
     return RA_ERR_WORKSPACE;
+  unsigned int* ew = nullptr;
+  st = error_word_or_refuse(&ew);
+  if (st != RA_OK) return st;
   const size_t base = ra_ring_forward_workspace_size(shp, c, layout, mode);
   const size_t eb = static_cast<size_t>(elem_bytes(shp.dtype));
   const size_t S = static_cast<size_t>(shp.Sq), B = static_cast<size_t>(shp.B), D = shp.D;

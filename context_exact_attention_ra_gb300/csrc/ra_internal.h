@@ -130,10 +130,20 @@ int decode_partials(int B, int Hkv, int G, int R, int pieces);
 bool decode_tc_applies(int D, int n, int layout);
 int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c);
 int launch_decode_tc(const DecodeParams& p, void* stream);
-unsigned int* device_error_word(int* cuda_err);
+// The device error word of the current device (its CUDA context), looked up
+// on first use in that context.  Two words after it the kernels find the
+// device address of the host mirror (or null), which they set when they raise
+// an error; `mirror` (may be null) receives the host view of that mirror.
+unsigned int* device_error_word(int* cuda_err, volatile unsigned int** mirror = nullptr);
+// A unique, nonzero identity of the calling thread's current CUDA context, or
+// 0 when there is none yet (caches of per-device handles are keyed by it, so
+// that a device reset, which ends the context, never leaves a stale handle).
+unsigned long long current_context_id();
 // Name of the host step that produced the last launcher error (thread-local).
 const char*& launch_stage();
-int read_and_clear_error(void* stream, unsigned int* value);
+// Wait for `stream`, read the device error word into *value and, when
+// `clear`, clear it and its host mirror.  Returns a cudaError_t value.
+int read_and_clear_error(void* stream, unsigned int* value, bool clear = true);
 int launch_selftest_timeout(unsigned int* err, uint64_t limit_ns, void* stream);
 
 // ---- host scheduler (ra_sched.cpp) ------------------------------------

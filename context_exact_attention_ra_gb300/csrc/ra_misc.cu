@@ -7,13 +7,16 @@
 
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "ra_internal.h"
 
 namespace ra {
 namespace {
 
-__device__ unsigned int g_error_word = 0;
+// The device error word (index 0) and, at byte offset 8, the device address
+// of its host mirror (null until the host registers one).
+__device__ __align__(16) unsigned int g_error_block[4] = {0u, 0u, 0u, 0u};
 
 __global__ void state_init_kernel(long long n_o, long long n_ml, float* o, float* m, float* l) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -433,31 +436,81 @@ const char*& launch_stage() {
   return stage;
 }
 
-unsigned int* device_error_word(int* cuda_err) {
-  // One address per device; looked up with that device current.
-  static unsigned int* cache[64] = {nullptr};
+namespace {
+// Host mirrors of the device error words: one 64-byte slot per device in one
+// page of this library's own memory, registered (pinned and mapped into every
+// device's address space) on first use.  The library allocates nothing for it.
+constexpr int kMaxDevices = 64;
+alignas(4096) unsigned int g_mirror_page[kMaxDevices * 16];
+
+struct ErrorHandles {
+  unsigned long long ctx = 0;
+  unsigned int* word = nullptr;
+  volatile unsigned int* mirror = nullptr;   // host view, or null
+};
+
+std::mutex g_error_mu;
+ErrorHandles g_error_cache[kMaxDevices];
+bool g_mirror_registered = false;
+bool g_mirror_failed = false;
+}  // namespace
+
+unsigned int* device_error_word(int* cuda_err, volatile unsigned int** mirror) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     *cuda_err = static_cast<int>(e != cudaSuccess ? e : cudaErrorInvalidDevice);
     return nullptr;
   }
-  if (cache[dev] == nullptr) {
+  std::lock_guard<std::mutex> lock(g_error_mu);
+  ErrorHandles& h = g_error_cache[dev];
+  const unsigned long long ctx = current_context_id();
+  if (h.word == nullptr || h.ctx != ctx) {
+    // first use in this context (or the context changed: a device reset
+    // ended the old one): look the word up with this device current, which
+    // also creates the context if none exists yet
     void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_error_word);
+    e = cudaGetSymbolAddress(&ptr, g_error_block);
     if (e != cudaSuccess) {
       *cuda_err = static_cast<int>(e);
       return nullptr;
     }
-    cache[dev] = static_cast<unsigned int*>(ptr);
+    h.word = static_cast<unsigned int*>(ptr);
+    h.mirror = nullptr;
+    // The mirror: best effort; without it the kernels still record errors in
+    // the device word, and only the host's early refusal is lost.
+    if (!g_mirror_registered && !g_mirror_failed) {
+      e = cudaHostRegister(g_mirror_page, sizeof(g_mirror_page),
+                           cudaHostRegisterPortable | cudaHostRegisterMapped);
+      if (e == cudaSuccess || e == cudaErrorHostMemoryAlreadyRegistered) {
+        g_mirror_registered = true;
+      } else {
+        g_mirror_failed = true;
+      }
+      cudaGetLastError();   // a failed registration must not linger as the last error
+    }
+    if (g_mirror_registered) {
+      unsigned int* slot = g_mirror_page + 16 * dev;
+      void* dslot = nullptr;
+      if (cudaHostGetDevicePointer(&dslot, slot, 0) == cudaSuccess && dslot != nullptr) {
+        // publish the mirror's device address next to the word (synchronous,
+        // once per context)
+        if (cudaMemcpy(h.word + 2, &dslot, sizeof(dslot), cudaMemcpyHostToDevice) == cudaSuccess)
+          h.mirror = slot;
+      }
+      cudaGetLastError();
+    }
+    h.ctx = current_context_id();
   }
   *cuda_err = 0;
-  return cache[dev];
+  if (mirror != nullptr) *mirror = h.mirror;
+  return h.word;
 }
 
-int read_and_clear_error(void* stream, unsigned int* value) {
+int read_and_clear_error(void* stream, unsigned int* value, bool clear) {
   int err = 0;
-  unsigned int* w = device_error_word(&err);
+  volatile unsigned int* mirror = nullptr;
+  unsigned int* w = device_error_word(&err, &mirror);
   if (w == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
@@ -465,11 +518,12 @@ int read_and_clear_error(void* stream, unsigned int* value) {
   unsigned int v = 0;
   e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return static_cast<int>(e);
-  if (v != 0) {
+  if (v != 0 && clear) {
     const unsigned int zero = 0;
     e = cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return static_cast<int>(e);
   }
+  if (mirror != nullptr && clear) *mirror = 0u;
   *value = v;
   return 0;
 }

@@ -22,8 +22,10 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "ra.h"
+#include "ra_internal.h"
 
 namespace {
 
@@ -33,10 +35,16 @@ constexpr int kMaxDevices = 64;
 
 // Device address of the scratch array for the current device.  In host code
 // the array's name only stands for it; the real address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current
-// (on the first call made on the device).
+// cudaGetSymbolAddress, looked up with that device current on the first call
+// in each CUDA context (a device reset ends the context, and the next call
+// looks the address up again rather than reusing one that no longer exists).
 void* scratch_address(cudaError_t* err) {
-  static void* cache[kMaxDevices] = {nullptr};
+  struct Entry {
+    unsigned long long ctx = 0;
+    void* ptr = nullptr;
+  };
+  static std::mutex mu;
+  static Entry cache[kMaxDevices];
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return nullptr;
@@ -44,13 +52,17 @@ void* scratch_address(cudaError_t* err) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
-  if (cache[dev] == nullptr) {
+  std::lock_guard<std::mutex> lock(mu);
+  Entry& e = cache[dev];
+  const unsigned long long ctx = ra::current_context_id();
+  if (e.ptr == nullptr || e.ctx != ctx) {
     void* ptr = nullptr;
     *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (*err != cudaSuccess) return nullptr;
-    cache[dev] = ptr;
+    e.ptr = ptr;
+    e.ctx = ra::current_context_id();
   }
-  return cache[dev];
+  return e.ptr;
 }
 
 }  // namespace

@@ -1,5 +1,7 @@
-// Host side of the TMA loads: tensor maps over [B][rows][H][D] bf16 tensors.
-// The CUDA driver API's cuTensorMapEncodeTiled is looked up once through the runtime.
+// Host side of the TMA loads: tensor maps over [B][rows][H][D] bf16 tensors;
+// and the identity of the current CUDA context.  The CUDA driver API's
+// cuTensorMapEncodeTiled, cuCtxGetCurrent and cuCtxGetId are looked up once
+// through the runtime.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -34,7 +36,42 @@ EncodeTiledFn encode_fn(int* err) {
   return fn;
 }
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct CtxFns {
+  CtxGetCurrentFn current = nullptr;
+  CtxGetIdFn id = nullptr;
+};
+
+const CtxFns& ctx_fns() {
+  static CtxFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess && f != nullptr)
+      fns.current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess && f != nullptr)
+      fns.id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  return fns;
+}
+
 }  // namespace
+
+unsigned long long current_context_id() {
+  const CtxFns& f = ctx_fns();
+  if (f.current == nullptr || f.id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (f.current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (f.id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id + 1;   // 0 stays free for "no context"
+}
 
 // Boxes of 64 columns (128 bytes, 128-byte swizzle) x 1 head x box_rows rows;
 // rows past the end of the tensor read as zeros.

@@ -22,6 +22,20 @@ struct Abort {
   unsigned int* err;      // global memory: the device error word
 };
 
+// Record an error: set `code` in the device error word and, when the host has
+// registered a mirror for this device (a word of pinned host memory mapped
+// into the device's address space, whose device address sits 8 bytes after
+// the error word), raise the mirror too, so that the host's entry points see
+// the pending error without synchronising.
+__device__ __forceinline__ void raise_error(unsigned int* err, unsigned int code) {
+  atomicOr(err, code);
+  unsigned int* mirror = *reinterpret_cast<unsigned int* volatile*>(err + 2);
+  if (mirror != nullptr) {
+    *reinterpret_cast<volatile unsigned int*>(mirror) = 1u;
+    __threadfence_system();
+  }
+}
+
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, Abort ab,
                                            unsigned int code, uint64_t limit_ns) {
   const uint64_t t0 = ptx::global_timer_ns();
@@ -37,7 +51,7 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, Abort 
       }
       if (ptx::global_timer_ns() - t0 > limit_ns) {
         *ab.flag = 1;
-        atomicOr(ab.err, code);
+        raise_error(ab.err, code);
         return false;
       }
     }

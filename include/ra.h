@@ -29,8 +29,9 @@
  *  - The causal mask is inclusive: query position p sees key position p'
  *    when p' <= p.
  *  - The caller owns every buffer.  The library never allocates device or
- *    pinned memory; where it needs scratch the caller passes a workspace of
- *    the size the matching *_workspace_size function returns.
+ *    pinned memory (it only registers one page of its own host memory, the
+ *    error mirror below); where it needs scratch the caller passes a workspace
+ *    of the size the matching *_workspace_size function returns.
  *  - Device pointers must be 16-byte aligned.  Positions are int32.
  *  - Calls are asynchronous and stream-ordered on the given stream (NULL is
  *    the legacy default stream), except where noted.  Arguments are checked
@@ -38,7 +39,17 @@
  *    returns RA_ERR_INVALID or RA_ERR_UNSUPPORTED and launches nothing.
  *  - Every device-side wait in the kernels is bounded.  A wait that runs out
  *    sets a device error word and the kernel returns early; ra_device_error()
- *    reports it as RA_ERR_TIMEOUT.
+ *    reports it as RA_ERR_TIMEOUT and clears it.  Until it is cleared, kernels
+ *    launched on that device return without computing anything, so every
+ *    entry point that launches work first reads a host-mapped mirror of the
+ *    word (no synchronisation) and, if an error is pending, returns
+ *    RA_ERR_TIMEOUT without launching.  Work already enqueued when a wait runs
+ *    out is not recalled: it finishes as a no-op, and only ra_device_error()
+ *    (or a call with a report) tells.  The mirror is one page of the
+ *    library's own host memory, registered with the CUDA driver on the first
+ *    call in a process; each device's first call also publishes its address
+ *    to the device with a synchronous copy, so make that first call before
+ *    any stream capture.
  *  - Nothing here is thread-safe across concurrent calls that share a
  *    workspace.
  */
@@ -323,10 +334,13 @@ ra_status ra_device_error(ra_stream_t stream);
  * a barrier that nothing ever arrives on.  The wait gives up after about
  * limit_us microseconds (1 .. 1000000; the check runs every 256 polls, so the
  * real time can be longer), sets its bit in the device error word and the
- * kernel returns.  Returns RA_ERR_TIMEOUT when the path works as designed (the
- * error word is cleared again), RA_ERR_INVALID for a bad limit, RA_ERR_CUDA if
- * a CUDA call fails.  The device stays usable afterwards. */
-ra_status ra_selftest_wait_timeout(uint32_t limit_us, ra_stream_t stream);
+ * kernel returns.  Returns RA_ERR_TIMEOUT when the path works as designed,
+ * RA_ERR_INVALID for a bad limit, RA_ERR_CUDA if a CUDA call fails.  With
+ * leave_pending == 0 the error word is cleared again before the return; with
+ * leave_pending != 0 it stays set, as after a real timeout, so that a caller
+ * can check that later calls are refused until ra_device_error() clears it.
+ * The device stays usable afterwards. */
+ra_status ra_selftest_wait_timeout(uint32_t limit_us, int leave_pending, ra_stream_t stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

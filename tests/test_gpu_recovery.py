@@ -55,6 +55,38 @@ def test_device_timeout_is_reported_and_the_device_stays_usable():
     parity.check_lse(_np(lse), ref_lse, "after the self-test")
 
 
+def test_pending_device_error_refuses_new_work_until_read():
+    """After a wait has run out, and before ra_device_error() has read it,
+    every entry point that launches work refuses with RA_ERR_TIMEOUT instead
+    of returning RA_OK over stale output; once the error is read and cleared,
+    the same calls compute the right result."""
+    w = small_case(1024, 2, "zigzag", True, B=1, Hq=4, Hkv=2, D=128, seed=33)
+    q, k, v, _ = make_inputs(w)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    assert ra.selftest_wait_timeout(2000, leave_pending=True) == ra.ERR_TIMEOUT
+    sentinel = torch.full(qd.shape, 7.0, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ra.RaError) as exc:
+        ra.ring_forward(qd, kd, vd, w.c, "zigzag", True, "fused", scale=w.scale, out=sentinel)
+    assert exc.value.status == ra.ERR_TIMEOUT
+    with pytest.raises(ra.RaError) as exc:
+        ra.state_init(1, 256, 4, 128)
+    assert exc.value.status == ra.ERR_TIMEOUT
+    torch.cuda.synchronize()
+    assert bool((sentinel == 7.0).all()), "a refused call wrote its output"
+    # the pending error is still there for ra_device_error to report, once
+    with pytest.raises(ra.RaError) as exc:
+        ra.device_error()
+    assert exc.value.status == ra.ERR_TIMEOUT
+    ra.device_error()
+    out, lse = ra.ring_forward(qd, kd, vd, w.c, "zigzag", True, "fused", scale=w.scale,
+                               out_dtype=torch.float32)
+    ra.device_error()
+    pos = np.arange(w.S)
+    ref, ref_lse, _, _ = oracle.attention_reference(_np(q), _np(k), _np(v), pos, pos, True, w.scale)
+    parity.check_bf16(_np(out), ref, "after the pending error was cleared")
+    parity.check_lse(_np(lse), ref_lse, "after the pending error was cleared")
+
+
 @pytest.mark.parametrize("layout,t_stop", [("zigzag", 1), ("contiguous", 3), ("striped", 2)])
 def test_ring_resumes_from_a_saved_state_bit_for_bit(layout, t_stop):
     S, c, rank = 2048, 4, 2

@@ -138,8 +138,8 @@ def test_expected_work_at_c16_reproduces_the_plate():
 
 
 def test_selftest_rejects_a_bad_limit_before_any_launch(lib):
-    assert lib.ra_selftest_wait_timeout(ctypes.c_uint32(0), ctypes.c_void_p(0)) == -1
-    assert lib.ra_selftest_wait_timeout(ctypes.c_uint32(2000000), ctypes.c_void_p(0)) == -1
+    assert lib.ra_selftest_wait_timeout(ctypes.c_uint32(0), 0, ctypes.c_void_p(0)) == -1
+    assert lib.ra_selftest_wait_timeout(ctypes.c_uint32(2000000), 1, ctypes.c_void_p(0)) == -1
 
 
 def test_other_entry_points_reject_bad_arguments_before_launch(lib):
