@@ -6,12 +6,9 @@ the computed (fp32) result; its final rounding to bf16 adds up to half a bf16
 ulp of the value (0.0156 for |out| in [4, 8)), more than 1e-2 on its own, so
 the rounded output is checked to be exactly the fp32 result rounded to
 nearest even instead (``check_rounding``); LSE within
-1e-3 absolute, |d| <= 1e-3, on every workload but the rescale stress one;
-there the logits reach O(1e3), one fp32 ulp of the LSE is 6e-5 and the fp32
-accumulation of a 128-term dot product of O(1e3) logits carries errors of
-that order, so the stress LSE is held to |d| <= 1e-3 * max(1, |lse|) and its
-strict absolute maximum is reported beside it; fp32 paths within 1e-5
-relative, read as max|d| / max|ref| <= 1e-5.
+1e-3 absolute, |d| <= 1e-3, on every workload, the rescale stress one
+included (its LSE reaches O(1e3); the largest error is printed there);
+fp32 paths within 1e-5 relative, read as max|d| / max|ref| <= 1e-5.
 """
 
 from __future__ import annotations
@@ -61,23 +58,18 @@ def check_bf16(out, ref, what=""):
     return float(d.max()), float(d.mean())
 
 
-def check_lse(lse, ref, what="", relative=False):
-    """|lse - ref| <= 1e-3 on every finite row (absolute).  relative=True is for
-    the rescale stress workload only: |d| <= 1e-3 * max(1, |ref|), with the
-    strict absolute maximum printed beside it."""
+def check_lse(lse, ref, what="", report=False):
+    """|lse - ref| <= 1e-3 on every finite row (absolute); `report` prints the
+    largest error and the largest |lse| of the rows checked."""
     lse = np.asarray(lse, dtype=np.float64)
     fin = np.isfinite(ref)
     assert (np.isfinite(lse) == fin).all(), f"{what}: lse finiteness differs"
     d = np.abs(lse[fin] - ref[fin])
     if not d.size:
         return 0.0
-    if relative:
-        bound = LSE_TOL * np.maximum(1.0, np.abs(ref[fin]))
-        print(f"{what}: lse strict absolute max {d.max():.3e} (bound {LSE_TOL:g} x max(1, |lse|); "
-              f"|lse| up to {np.abs(ref[fin]).max():.1f})")
-    else:
-        bound = np.full(d.shape, LSE_TOL)
-    assert (d <= bound).all(), f"{what}: lse max {d.max():.3e} (worst ratio {(d / bound).max():.3f})"
+    if report:
+        print(f"{what}: lse max |d| {d.max():.3e} (|lse| up to {np.abs(ref[fin]).max():.1f})")
+    assert d.max() <= LSE_TOL, f"{what}: lse max |d| {d.max():.3e} > {LSE_TOL}"
     return float(d.max())
 
 

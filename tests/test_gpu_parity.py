@@ -147,7 +147,7 @@ def test_large_workloads_sampled_rows(name, layout):
     got = _np(out32[:, torch.as_tensor(rows)])
     parity.check_bf16(got, ref, f"{name}/{layout} out")
     parity.check_lse(_np(lse[:, :, torch.as_tensor(rows)]), ref_lse, f"{name}/{layout} lse",
-                     relative=(name == "stress"))
+                     report=True)
     # properties that hold for every row: finite, and |out| bounded by max |v|
     o = out32
     assert torch.isfinite(o).all()
