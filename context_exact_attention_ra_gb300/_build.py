@@ -24,7 +24,7 @@ LIB = os.path.join(HERE, "libra_gb300.so")
 
 SOURCES = ["ra_api.cpp", "ra_sched.cpp", "ra_misc.cu", "attn_f32.cu", "attn_tc_sm103.cu",
            "decode_attn.cu", "ra_noalloc.cu", "ra_selftest.cu", "ra_tma.cpp",
-           "decode_tc_sm103.cu"]
+           "decode_tc_sm103.cu", "attn_pair_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -752,7 +752,8 @@ int launch_d(const AttnParams& p, const void* q, const void* k, const void* v,
 int launch_attn_tc(const AttnParams& p, const void* q, const void* k, const void* v,
                    long long q_rows_total, long long k_rows_total, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p.D == 128) return launch_d<128>(p, q, k, v, q_rows_total, k_rows_total, s);
+  // D = 128 runs on SM pairs (attn_pair_sm103.cu); D = 64 on single CTAs
+  if (p.D == 128) return launch_attn_pair(p, q, k, v, q_rows_total, k_rows_total, stream);
   if (p.D == 64) return launch_d<64>(p, q, k, v, q_rows_total, k_rows_total, s);
   return static_cast<int>(cudaErrorInvalidValue);
 }

@@ -64,8 +64,8 @@ ra_status check_shape(const ra_shape& s) {
   if (s.dtype != RA_BF16 && s.dtype != RA_F32) return RA_ERR_UNSUPPORTED;
   if (s.D != 64 && s.D != 128) return RA_ERR_UNSUPPORTED;
   if (!std::isfinite(s.scale) || !(s.scale > 0.f)) return RA_ERR_INVALID;
-  // Index arithmetic in the kernels is 64-bit; grid x holds B*Hq.
-  if (static_cast<long long>(s.B) * s.Hq > 0x7fffffffLL) return RA_ERR_UNSUPPORTED;
+  // Index arithmetic in the kernels is 64-bit; grid x holds 2*B*Hq (CTA pairs).
+  if (static_cast<long long>(s.B) * s.Hq > 0x3fffffffLL) return RA_ERR_UNSUPPORTED;
   return RA_OK;
 }
 
@@ -91,10 +91,16 @@ bool out_dtype_ok(const ra_shape& s, int out_dtype) {
   return out_dtype == s.dtype || out_dtype == RA_F32;
 }
 
-int rows_per_block(int dtype) { return dtype == RA_BF16 ? ra::kPairRows : ra::kTile; }
+// Query rows per thread block of the attention kernel the shape runs on: the
+// CTA-pair kernel (bf16, D = 128), the single-CTA tensor-core kernel (bf16,
+// D = 64) or the exact fp32 kernel.
+int rows_per_block(const ra_shape& s) {
+  if (s.dtype != RA_BF16) return ra::kTile;
+  return s.D == 128 ? ra::kPairBlockRows : ra::kPairRows;
+}
 
 int blocks_per_rank(const ra_shape& s, int n_q) {
-  const int rpb = rows_per_block(s.dtype);
+  const int rpb = rows_per_block(s);
   return (n_q + rpb - 1) / rpb;
 }
 
@@ -298,7 +304,7 @@ ra_status ra_ring_prepare(const void* q, const void* k, const void* v, ra_shape 
   // Heavy-first block order (used by causal calls): depends on positions only.
   const int total_blocks = c * blocks_per_rank(shp, n);
   if (total_blocks > 1 && total_blocks <= ra::kMaxOrderedBlocks) {
-    e = ra::launch_block_order(at<int32_t>(workspace, w.pos), c, n, rows_per_block(shp.dtype),
+    e = ra::launch_block_order(at<int32_t>(workspace, w.pos), c, n, rows_per_block(shp),
                                blocks_per_rank(shp, n), at<int32_t>(workspace, w.order), stream);
     if (e) return cuda_fail(e, ra::launch_stage());
   }
@@ -864,7 +870,7 @@ ra_status hostio_pipelined(const void* q_host, const void* k_src, const void* v_
                           at<int32_t>(workspace, w.pos), s);
   if (!e) e = ra::launch_tile_ranges(at<int32_t>(workspace, w.pos), c, n, at<int2>(workspace, w.ranges), s);
   if (!e)
-    e = ra::launch_block_order(at<int32_t>(workspace, w.pos), c, n, rows_per_block(shp.dtype), bpr,
+    e = ra::launch_block_order(at<int32_t>(workspace, w.pos), c, n, rows_per_block(shp), bpr,
                                at<int32_t>(workspace, w.order), s, 1);
   if (e) return cuda_fail(e, ra::launch_stage());
   ce = cudaEventRecord(e_prep, s);

@@ -13,7 +13,8 @@
 namespace ra {
 
 constexpr int kTile = 128;        // query rows and keys per tile
-constexpr int kPairRows = 256;    // query rows per tensor-core block (two tiles)
+constexpr int kPairRows = 256;    // query rows per single-CTA tensor-core block (two tiles, D = 64)
+constexpr int kPairBlockRows = 512;   // query rows per CTA-pair block (two tiles per CTA, D = 128)
 constexpr int kMaxOrderedBlocks = 12288;  // heavy-first ordering limit (48 KB of keys)
 
 // Parameters of one launch of the attention kernels (both the tensor-core
@@ -101,6 +102,9 @@ int make_tma_map_bf16(CUtensorMap* map, const void* base, int B, long long rows,
                       int box_rows);
 int launch_attn_tc(const AttnParams& p, const void* q, const void* k, const void* v,
                    long long q_rows_total, long long k_rows_total, void* stream);
+// The same on clusters of two CTAs (pair MMAs), D = 128 (attn_pair_sm103.cu).
+int launch_attn_pair(const AttnParams& p, const void* q, const void* k, const void* v,
+                     long long q_rows_total, long long k_rows_total, void* stream);
 int launch_attn_f32(const AttnParams& p, void* stream);
 int launch_state_init(int B, int rows, int Hq, int D, float* o, float* m, float* l, void* stream);
 int launch_pack(const void* q, const void* k, const void* v, int B, int S, int Hq, int Hkv,
