@@ -91,7 +91,7 @@ def load_peaks():
 def kernel_traffic(kernel_src):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "attn_fwd_tc_s128k_traffic.json")
+    path = os.path.join(ROOT, "profiles", "attn_fwd_pair_s128k_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
@@ -294,9 +294,9 @@ def run_ours(args, rank, world, local):
     achieved = flop / (attn_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": kernel_traffic("attn_tc_sm103.cu") if md == ra.MODE_FUSED else None,
-            "kernel": {ra.MODE_FUSED: "attn_fwd_tc_kernel<128>",
-                       ra.MODE_ALLGATHER: "attn_fwd_tc_kernel<128> (one step over the gathered keys)"}.get(
+            "frac": achieved / peak, "traffic": kernel_traffic("attn_pair_sm103.cu") if md == ra.MODE_FUSED else None,
+            "kernel": {ra.MODE_FUSED: "attn_fwd_pair_kernel (CTA pairs, D = 128)",
+                       ra.MODE_ALLGATHER: "attn_fwd_pair_kernel (one step over the gathered keys)"}.get(
                            md, "attend (per-step launches + merge)"),
             "peak_source": f"{peak_kind} bf16_tflops (burst)",
             "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),

@@ -531,13 +531,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         unsigned int nvis = static_cast<unsigned int>(k.valid);
         if (masked && p.k_sorted) {
           // positions increase inside the tile: the visible keys are the prefix
-          // of those at or before this row's position (binary search)
+          // of those at or before this row's position.  Equally spaced
+          // positions (consecutive, or every c-th in striped shards) give the
+          // count directly from the tile's (min, max); otherwise binary search.
           int cnt = k.valid;
           if (p.causal) {
-            cnt = 0;
+            const int span = k.mx - k.mn;
+            if (qpos < k.mn) {
+              cnt = 0;
+            } else if (span == k.valid - 1) {
+              cnt = min(k.valid, qpos - k.mn + 1);
+            } else if (p.k_stride > 1 && span == (k.valid - 1) * p.k_stride) {
+              cnt = min(k.valid, (qpos - k.mn) / p.k_stride + 1);
+            } else {
+              cnt = 0;
 #pragma unroll
-            for (int step = 128; step > 0; step >>= 1)
-              if (cnt + step <= k.valid && __ldg(kp + cnt + step - 1) <= qpos) cnt += step;
+              for (int step = 128; step > 0; step >>= 1)
+                if (cnt + step <= k.valid && __ldg(kp + cnt + step - 1) <= qpos) cnt += step;
+            }
           }
           nvis = static_cast<unsigned int>(cnt);
 #pragma unroll

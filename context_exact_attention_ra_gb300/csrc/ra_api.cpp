@@ -333,6 +333,7 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
   const int n = S / c;
   AttnParams p = base_params(shp, c, n, n, causal);
   p.k_sorted = 1;   // shard rows are in increasing position in every layout
+  p.k_stride = (layout == RA_STRIPED) ? c : 1;
   p.q_pos = at<int32_t>(workspace, w.pos);
   p.k_pos = p.q_pos;
   p.k_ranges = at<int2>(workspace, w.ranges);
@@ -645,6 +646,7 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
 
   AttnParams p = base_params(shp, c, n, n, causal);
   p.k_sorted = 1;   // shard rows are in increasing position in every layout
+  p.k_stride = (layout == RA_STRIPED) ? c : 1;
   p.q_pos = at<int32_t>(workspace, w.pos);
   p.k_pos = p.q_pos;
   p.k_ranges = at<int2>(workspace, w.ranges);
@@ -882,6 +884,7 @@ ra_status hostio_pipelined(const void* q_host, const void* k_src, const void* v_
   if (ew == nullptr) return cuda_fail(err, "device error word lookup");
   AttnParams p = base_params(shp, c, n, n, causal);
   p.k_sorted = 1;
+  p.k_stride = (layout == RA_STRIPED) ? c : 1;
   p.q_pos = at<int32_t>(workspace, w.pos);
   p.k_pos = p.q_pos;
   p.k_ranges = at<int2>(workspace, w.ranges);

@@ -32,6 +32,9 @@ struct AttnParams {
                                //    own layouts), so a row's visible keys in a tile are a prefix
   int kv_by_holder;            // 1: the block held at a step sits in the holder's slot of k, v
                                //    (rows rank*n_k ..), its positions are the source's
+  int k_stride;                // > 1: key positions inside a tile may step by this much (striped
+                               //    shards: c); a tile whose (min, max) span is (count - 1) * stride
+                               //    (or count - 1) holds equally spaced positions
   int q_blocks_per_rank;       // ceil(n_q / rows per block)
   int causal;
   float scale_log2;            // scale * log2(e)
