@@ -22,7 +22,8 @@
 // instruction costs the tensor core the same for any N up to 128), added in
 // the epilogue.  Every thread also owns one output column of O^T and rescales it
 // when a row's maximum rose.  K and V tiles stream through three shared-memory
-// stages by TMA, so the block reads each key and value byte once, and the
+// stages by TMA (a striped shard's keys, every c-th row, through a 5-D view of
+// the tensor), so the block reads each key and value byte once, and the
 // kernel is bound by HBM bandwidth; the loads carry an evict-first L2 policy,
 // so that the stream displaces its own lines rather than whatever else L2
 // holds (often lines that would first have to be written back).
@@ -247,13 +248,23 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         if (!ok) break;
         int shard, lt;
         tile_of(j, shard, lt);
-        const int nat0 = static_cast<int>(dt_natural_key(shard, lt * kDTKeys, p.n, p.c, p.layout));
         ptx::mbar_arrive_expect_tx(bar(L::bKVFull + st), 2 * L::kKVTile);
-        for (int x = 0; x < 2; ++x) {
-          ptx::tma_load_4d_hint(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
-                                x * L::kBox, g, nat0, b, pol);
-          ptx::tma_load_4d_hint(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
-                                x * L::kBox, g, nat0, b, pol);
+        if (p.layout == RA_STRIPED) {
+          // every c-th key: (column, head, shard, index in shard, batch)
+          for (int x = 0; x < 2; ++x) {
+            ptx::tma_load_5d_hint(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
+                                  x * L::kBox, g, shard, lt * kDTKeys, b, pol);
+            ptx::tma_load_5d_hint(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
+                                  x * L::kBox, g, shard, lt * kDTKeys, b, pol);
+          }
+        } else {
+          const int nat0 = static_cast<int>(dt_natural_key(shard, lt * kDTKeys, p.n, p.c, p.layout));
+          for (int x = 0; x < 2; ++x) {
+            ptx::tma_load_4d_hint(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
+                                  x * L::kBox, g, nat0, b, pol);
+            ptx::tma_load_4d_hint(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
+                                  x * L::kBox, g, nat0, b, pol);
+          }
         }
         ++issued;
       }
@@ -483,7 +494,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
 
 bool decode_tc_applies(int D, int n, int layout) {
   if (D != kDTD || n <= 0) return false;
-  if (layout == RA_CONTIGUOUS) return true;
+  if (layout == RA_CONTIGUOUS || layout == RA_STRIPED) return true;
   return layout == RA_ZIGZAG && (n / 2) % kDTKeys == 0;
 }
 
@@ -503,8 +514,14 @@ int launch_decode_tc(const DecodeParams& p, void* stream) {
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
   launch_stage() = "cuTensorMapEncodeTiled (decode)";
-  int e = make_tma_map_bf16(&mk, p.k, p.B, p.S, p.Hkv, kDTD, kDTKeys);
-  if (!e) e = make_tma_map_bf16(&mv, p.v, p.B, p.S, p.Hkv, kDTD, kDTKeys);
+  int e = 0;
+  if (p.layout == RA_STRIPED) {
+    e = make_tma_map_bf16_strided(&mk, p.k, p.B, p.S, p.Hkv, kDTD, p.c, kDTKeys);
+    if (!e) e = make_tma_map_bf16_strided(&mv, p.v, p.B, p.S, p.Hkv, kDTD, p.c, kDTKeys);
+  } else {
+    e = make_tma_map_bf16(&mk, p.k, p.B, p.S, p.Hkv, kDTD, kDTKeys);
+    if (!e) e = make_tma_map_bf16(&mv, p.v, p.B, p.S, p.Hkv, kDTD, kDTKeys);
+  }
   if (e) return e;
   static int done[64] = {0};
   int dev = 0;

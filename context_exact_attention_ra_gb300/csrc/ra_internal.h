@@ -103,6 +103,9 @@ enum : unsigned int {
 // box_rows rows, 128-byte swizzle (ra_tma.cpp).  Returns a cudaError_t value.
 int make_tma_map_bf16(CUtensorMap* map, const void* base, int B, long long rows, int H, int D,
                       int box_rows);
+// The keys of striped shard r (rows r, r + c, ...) as a 5-D view {D, H, c, S / c, B}.
+int make_tma_map_bf16_strided(CUtensorMap* map, const void* base, int B, long long S, int H, int D, int c,
+                              int box_rows);
 int launch_attn_tc(const AttnParams& p, const void* q, const void* k, const void* v,
                    long long q_rows_total, long long k_rows_total, void* stream);
 // The same on clusters of two CTAs (pair MMAs), D = 128 (attn_pair_sm103.cu).
@@ -132,8 +135,9 @@ int decode_pieces_per_shard(int n);
 // Number of partial states (blocks per batch, key/value head and row block).
 int decode_partials(int B, int Hkv, int G, int R, int pieces);
 // The tensor-core decode (decode_tc_sm103.cu): D = 128 and 128-key tiles that
-// are contiguous in natural order (contiguous shards, or zig-zag chunks of a
-// multiple of 128 keys); otherwise the warp-level kernel runs.
+// one TMA box can load (contiguous shards, striped shards through a strided
+// view, zig-zag chunks of a multiple of 128 keys); otherwise the warp-level
+// kernel runs.
 bool decode_tc_applies(int D, int n, int layout);
 int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c);
 int launch_decode_tc(const DecodeParams& p, void* stream);

@@ -92,4 +92,27 @@ int make_tma_map_bf16(CUtensorMap* map, const void* base, int B, long long rows,
   return r == CUDA_SUCCESS ? 0 : static_cast<int>(cudaErrorInvalidValue);
 }
 
+// The rows r, r + c, r + 2c, ... of a [B][S][H][D] bf16 tensor (the keys of
+// striped shard r) as dimension 3 of a 5-D view {D, H, c, S / c, B}: a box of
+// 64 columns x 1 head x 1 shard x box_rows rows x 1 loads box_rows keys of one
+// shard; rows past S / c read as zeros.
+int make_tma_map_bf16_strided(CUtensorMap* map, const void* base, int B, long long S, int H, int D, int c,
+                              int box_rows) {
+  int err = 0;
+  EncodeTiledFn fn = encode_fn(&err);
+  if (fn == nullptr) return err ? err : static_cast<int>(cudaErrorNotSupported);
+  if (c <= 0 || S % c != 0) return static_cast<int>(cudaErrorInvalidValue);
+  const cuuint64_t row = static_cast<cuuint64_t>(H) * D * 2;
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(c),
+                        static_cast<cuuint64_t>(S / c), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[4] = {static_cast<cuuint64_t>(D) * 2, row, row * static_cast<cuuint64_t>(c),
+                           row * static_cast<cuuint64_t>(S)};
+  cuuint32_t box[5] = {64, 1, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(cudaErrorInvalidValue);
+}
+
 }  // namespace ra

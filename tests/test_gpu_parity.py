@@ -407,7 +407,9 @@ def test_allgather_large_sampled_rows():
 @pytest.mark.parametrize("S,c,layout,R,Hq,Hkv,D,B", [
     (4096, 4, "zigzag", 1, 8, 2, 128, 1),        # one new token, GQA 4:1
     (4096, 4, "contiguous", 4, 8, 2, 128, 2),    # a few tokens at mixed positions, batch 2
-    (3000, 5, "striped", 3, 6, 3, 64, 1),        # ragged pieces, D = 64
+    (3000, 5, "striped", 3, 6, 3, 64, 1),        # ragged pieces, D = 64 (warp-level kernel)
+    (3000, 5, "striped", 3, 6, 3, 128, 1),       # striped shards on the tensor cores, ragged last tile
+    (8192, 4, "striped", 1, 16, 1, 128, 2),      # striped, every tile full, batch 2
     (131072, 16, "zigzag", 1, 16, 1, 128, 1),    # the s128k shape: 16 query heads share one KV head
 ])
 def test_decode_split_kv_full_parity(S, c, layout, R, Hq, Hkv, D, B):
