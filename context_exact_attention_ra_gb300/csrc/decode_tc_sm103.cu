@@ -168,13 +168,24 @@ __global__ void __launch_bounds__(kDTThreads, 1)
   const int pi = blockIdx.y;
   const int row0 = rb * kDTRows;
   const int nrows = min(kDTRows, rows - row0);
-  const int tps = (p.n + kDTKeys - 1) / kDTKeys;   // tiles per shard
+  // A shard is one stretch of the natural order (contiguous; striped through
+  // the strided view) or two (zig-zag chunks); each stretch is cut into
+  // 128-key tiles of its own, so that every tile is one TMA box.
+  const int np = (p.layout == RA_ZIGZAG) ? 2 : 1;   // stretches per shard
+  const int pl = p.n / np;                          // keys per stretch
+  const int tpp = (pl + kDTKeys - 1) / kDTKeys;     // tiles per stretch
+  const int tps = np * tpp;                         // tiles per shard
   const int T = p.c * tps;
   const int J = (pi < T) ? (T - 1 - pi) / p.P + 1 : 0;   // tiles of this block
-  auto tile_of = [&](int j, int& shard, int& lt) {
+  // tile j of this block: its shard, the shard-local index of its first key,
+  // and its number of keys
+  auto tile_of = [&](int j, int& shard, int& i0, int& len) {
     const int ti = pi + j * p.P;
     shard = ti / tps;
-    lt = ti % tps;
+    const int rem = ti % tps;
+    const int lt = rem % tpp;
+    i0 = (rem / tpp) * pl + lt * kDTKeys;
+    len = min(kDTKeys, pl - lt * kDTKeys);
   };
 
   // ---- set-up --------------------------------------------------------------
@@ -246,19 +257,19 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         const int st = j % kDTStages;
         if (j >= kDTStages) ok = wait_bar(bar(L::bKVEmpty + st), ((j / kDTStages) - 1) & 1u, ab, kErrTimeoutEmpty);
         if (!ok) break;
-        int shard, lt;
-        tile_of(j, shard, lt);
+        int shard, i0, len;
+        tile_of(j, shard, i0, len);
         ptx::mbar_arrive_expect_tx(bar(L::bKVFull + st), 2 * L::kKVTile);
         if (p.layout == RA_STRIPED) {
           // every c-th key: (column, head, shard, index in shard, batch)
           for (int x = 0; x < 2; ++x) {
             ptx::tma_load_5d_hint(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
-                                  x * L::kBox, g, shard, lt * kDTKeys, b, pol);
+                                  x * L::kBox, g, shard, i0, b, pol);
             ptx::tma_load_5d_hint(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
-                                  x * L::kBox, g, shard, lt * kDTKeys, b, pol);
+                                  x * L::kBox, g, shard, i0, b, pol);
           }
         } else {
-          const int nat0 = static_cast<int>(dt_natural_key(shard, lt * kDTKeys, p.n, p.c, p.layout));
+          const int nat0 = static_cast<int>(dt_natural_key(shard, i0, p.n, p.c, p.layout));
           for (int x = 0; x < 2; ++x) {
             ptx::tma_load_4d_hint(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
                                   x * L::kBox, g, nat0, b, pol);
@@ -366,11 +377,10 @@ __global__ void __launch_bounds__(kDTThreads, 1)
       ptx::tc_fence_after_sync();
       uint32_t su[16];
       ptx::tmem_ld16(tmem + lane_base + sb * kDTRows, su);
-      int shard, lt;
-      tile_of(j, shard, lt);
-      const int i = lt * kDTKeys + t;
-      const bool kvalid = i < p.n;
-      const long long pos = dt_natural_key(shard, kvalid ? i : 0, p.n, p.c, p.layout);
+      int shard, i0, len;
+      tile_of(j, shard, i0, len);
+      const bool kvalid = t < len;   // rows past the stretch belong to another stretch or lie past the tensor
+      const long long pos = dt_natural_key(shard, i0 + (kvalid ? t : 0), p.n, p.c, p.layout);
       float x[kDTRows];
 #pragma unroll
       for (int n = 0; n < kDTRows; ++n) {
@@ -493,13 +503,13 @@ __global__ void __launch_bounds__(kDTThreads, 1)
 }  // namespace
 
 bool decode_tc_applies(int D, int n, int layout) {
-  if (D != kDTD || n <= 0) return false;
-  if (layout == RA_CONTIGUOUS || layout == RA_STRIPED) return true;
-  return layout == RA_ZIGZAG && (n / 2) % kDTKeys == 0;
+  (void)layout;
+  return D == kDTD && n > 0;
 }
 
-int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c) {
-  const long long tiles = static_cast<long long>(c) * ((n + kDTKeys - 1) / kDTKeys);
+int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c, int layout) {
+  const int np = (layout == RA_ZIGZAG) ? 2 : 1;
+  const long long tiles = static_cast<long long>(c) * np * ((n / np + kDTKeys - 1) / kDTKeys);
   const long long units = static_cast<long long>(B) * Hkv * ((static_cast<long long>(G) * R + kDTRows - 1) / kDTRows);
   long long want = (kDTTargetBlocks + units - 1) / units;
   if (want < 1) want = 1;

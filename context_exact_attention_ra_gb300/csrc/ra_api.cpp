@@ -537,7 +537,7 @@ DecodeWs decode_ws(const ra_shape& s, int c, int layout) {
   DecodeWs w;
   const int n = s.Sk / c;
   w.P = ra::decode_tc_applies(s.D, n, layout)
-            ? ra::decode_tc_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, n, c)
+            ? ra::decode_tc_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, n, c, layout)
             : ra::decode_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, c * ra::decode_pieces_per_shard(n));
   const size_t P = static_cast<size_t>(w.P), B = static_cast<size_t>(s.B), R = static_cast<size_t>(s.Sq);
   size_t off = 0;

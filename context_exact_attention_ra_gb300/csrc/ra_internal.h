@@ -134,12 +134,11 @@ int launch_decode(const DecodeParams& p, void* stream);
 int decode_pieces_per_shard(int n);
 // Number of partial states (blocks per batch, key/value head and row block).
 int decode_partials(int B, int Hkv, int G, int R, int pieces);
-// The tensor-core decode (decode_tc_sm103.cu): D = 128 and 128-key tiles that
-// one TMA box can load (contiguous shards, striped shards through a strided
-// view, zig-zag chunks of a multiple of 128 keys); otherwise the warp-level
-// kernel runs.
+// The tensor-core decode (decode_tc_sm103.cu): D = 128, every layout (each
+// contiguous stretch of a shard tiled on its own, striped shards through a
+// strided view); D = 64 runs the warp-level kernel.
 bool decode_tc_applies(int D, int n, int layout);
-int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c);
+int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c, int layout);
 int launch_decode_tc(const DecodeParams& p, void* stream);
 // The device error word of the current device (its CUDA context), looked up
 // on first use in that context.  Two words after it the kernels find the

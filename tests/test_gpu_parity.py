@@ -410,6 +410,9 @@ def test_allgather_large_sampled_rows():
     (3000, 5, "striped", 3, 6, 3, 64, 1),        # ragged pieces, D = 64 (warp-level kernel)
     (3000, 5, "striped", 3, 6, 3, 128, 1),       # striped shards on the tensor cores, ragged last tile
     (8192, 4, "striped", 1, 16, 1, 128, 2),      # striped, every tile full, batch 2
+    (3000, 5, "zigzag", 3, 6, 3, 128, 1),        # zig-zag chunks of 300 keys: two ragged tiles per shard
+    (6200, 4, "zigzag", 2, 8, 1, 128, 2),        # chunks of 775 keys, batch 2
+    (2600, 4, "contiguous", 2, 8, 2, 64, 1),     # D = 64 (warp-level kernel), contiguous
     (131072, 16, "zigzag", 1, 16, 1, 128, 1),    # the s128k shape: 16 query heads share one KV head
 ])
 def test_decode_split_kv_full_parity(S, c, layout, R, Hq, Hkv, D, B):
