@@ -20,16 +20,20 @@
 // Heads and remainders are stacked as the operand's 32 rows, so one N = 32
 // product per 16 keys accumulates both into separate columns of O^T (an
 // instruction costs the tensor core the same for any N up to 128), added in
-// the epilogue.  Every thread also owns one output column of O^T and rescales it
-// when a row's maximum rose.  K and V tiles stream through three shared-memory
+// the epilogue.  Every thread also owns one output column of O^T.  Two such
+// softmax pipelines (warps 0-3 and 4-7) take the block's tiles in turn, each
+// with its own S and P buffers, O^T accumulator and online-softmax state, so
+// that one works on a tile while the other's product runs; their two states
+// are merged at the end of the block.  K and V tiles stream through three shared-memory
 // stages by TMA (a striped shard's keys, every c-th row, through a 5-D view of
 // the tensor), so the block reads each key and value byte once, and the
 // kernel is bound by HBM bandwidth; the loads carry an evict-first L2 policy,
 // so that the stream displaces its own lines rather than whatever else L2
 // holds (often lines that would first have to be written back).
 //
-// Warp roles (192 threads): warps 0-3 softmax and epilogue, warp 4 TMA loads,
-// warp 5 tensor-memory allocation; its lane 0 issues the MMAs.  Every wait is
+// Warp roles (320 threads): warps 0-3 and 4-7 the two softmax pipelines
+// (even and odd tiles), warp 8 TMA loads, warp 9 tensor-memory allocation;
+// its lane 0 issues the MMAs.  Every wait is
 // bounded (ra_wait.cuh).
 
 #include <cuda.h>
@@ -51,10 +55,10 @@ constexpr int kDTRows = 16;           // query rows per block: the MMAs' N
 constexpr int kDTKeys = 128;          // keys per tile
 constexpr int kDTD = 128;             // head dimension of this kernel
 constexpr int kDTStages = 3;
-constexpr int kDTWarpLoad = 4;
-constexpr int kDTWarpMma = 5;
-constexpr int kDTThreads = 6 * 32;
-constexpr uint32_t kDTTmemCols = 64;  // S0 | S1 | O heads | O remainders, 16 columns each
+constexpr int kDTWarpLoad = 8;
+constexpr int kDTWarpMma = 9;
+constexpr int kDTThreads = 10 * 32;
+constexpr uint32_t kDTTmemCols = 128;  // S0 | S1 (16 columns each) | O0 | O1 (heads, remainders: 32 each)
 constexpr int kDTTargetBlocks = 152;  // one resident block per SM
 
 struct DTSmem {
@@ -78,8 +82,10 @@ struct DTSmem {
   static constexpr int bDrain = bXch + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;          // tmem slot, abort flag
-  static constexpr int kRed = kMisc + 16;                    // [2][4 warps][16] floats
-  static constexpr int kBytes = kRed + 2 * 4 * kDTRows * 4;
+  static constexpr int kRed = kMisc + 16;                    // [2 pipelines][4 warps][16] floats
+  static constexpr int kComb = kRed + 2 * 4 * kDTRows * 4;   // [2 pipelines][m, l][16] floats
+  static constexpr int kQpos = kComb + 2 * 2 * kDTRows * 4;  // [16] ints: the rows' positions
+  static constexpr int kBytes = kQpos + kDTRows * 4;
   static constexpr int kDynamic = kBytes + 1024;
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kP % 1024 == 0, "swizzle atoms are 1024 bytes");
   static_assert(kDynamic <= 232448, "shared memory budget");
@@ -213,15 +219,12 @@ __global__ void __launch_bounds__(kDTThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kDTTmemCols);
     ptx::tmem_relinquish();
   }
+  // the rows' query positions (rows past the block's rows: none visible)
+  int* const sqpos = reinterpret_cast<int*>(smem + L::kQpos);
+  if (threadIdx.x < kDTRows)
+    sqpos[threadIdx.x] = (static_cast<int>(threadIdx.x) < nrows) ? p.q_pos[(row0 + threadIdx.x) % p.R] : INT_MIN;
   // Q: 16 rows x 128 columns, K-major with the 128-byte swizzle; row
   // n = (head within group) * R + token, rows past the block's rows are zero.
-  int qpos[kDTRows];
-  bool rvalid[kDTRows];
-#pragma unroll
-  for (int n = 0; n < kDTRows; ++n) {
-    rvalid[n] = n < nrows;
-    qpos[n] = rvalid[n] ? p.q_pos[(row0 + n) % p.R] : INT_MIN;
-  }
   if (warp < 4) {
     const int t = threadIdx.x;
     const int n = t >> 3;              // row
@@ -313,10 +316,11 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         const uint64_t pd = dP + static_cast<uint64_t>((pb * L::kPBuf) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kDTKeys / 16; ++kk) {
-          // N = 32: the heads of P into O's first 16 columns, the remainders into the next 16
+          // N = 32: the heads of P into O's first 16 columns, the remainders
+          // into the next 16; tiles of each parity accumulate into their own O
           const uint64_t oa = static_cast<uint64_t>((kk * 16 * 128) >> 4);
           const uint64_t ob = static_cast<uint64_t>(((kk / 4) * L::kPBox + (kk % 4) * 32) >> 4);
-          ptx::tc_mma_ss(tmem + 2 * kDTRows, vd + oa, pd + ob, idPV, 1u);
+          ptx::tc_mma_ss(tmem + 2 * kDTRows + pb * 2 * kDTRows, vd + oa, pd + ob, idPV, 1u);
         }
       };
       for (int j = 0; j < J && ok; ++j) {
@@ -352,9 +356,14 @@ __global__ void __launch_bounds__(kDTThreads, 1)
     __syncwarp();
   } else {
     // ===================== softmax: thread t owns key t of each tile ========
-    const int t = threadIdx.x;                        // also the output column of O^T
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tO = tmem + lane_base + 2 * kDTRows;
+    // Pipeline sb takes tiles sb, sb + 2, ...: its S and P buffers, its O^T
+    // accumulator and its barriers are those of index sb.
+    const int sb = warp >> 2;
+    const int t = threadIdx.x & 127;                  // also the output column of O^T
+    const int wq = warp & 3;                          // TMEM lane quadrant
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + sb * kDTRows;
+    const uint32_t tO = tmem + lane_base + 2 * kDTRows + sb * 2 * kDTRows;
     {
       uint32_t z[32];
 #pragma unroll
@@ -369,76 +378,79 @@ __global__ void __launch_bounds__(kDTThreads, 1)
       lpart[n] = 0.f;
     }
     const float sl2 = p.scale_log2;
+    int qmin = INT_MAX;
+    for (int n = 0; n < nrows; ++n) qmin = min(qmin, sqpos[n]);
+    float* const rbuf = red + sb * 4 * kDTRows;
+    uint8_t* const pbuf = smem + L::kP + sb * L::kPBuf;
     bool ok = true;
-    for (int j = 0; j < J && ok; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bSFull + sb), (j >> 1) & 1u, ab, kErrTimeoutS));
-      if (!ok) break;
-      ptx::tc_fence_after_sync();
-      uint32_t su[16];
-      ptx::tmem_ld16(tmem + lane_base + sb * kDTRows, su);
+    int k = 0;                                        // tiles this pipeline has taken
+    for (int j = sb; j < J && ok; j += 2, ++k) {
+      // where this tile's keys sit (worked out while its S is still on the way)
       int shard, i0, len;
       tile_of(j, shard, i0, len);
       const bool kvalid = t < len;   // rows past the stretch belong to another stretch or lie past the tensor
       const long long pos = dt_natural_key(shard, i0 + (kvalid ? t : 0), p.n, p.c, p.layout);
+      // the whole tile visible to every row (the common case): no per-key test
+      const bool all_vis = (len == kDTKeys) &&
+                           (!p.causal || dt_natural_key(shard, i0 + len - 1, p.n, p.c, p.layout) <= qmin);
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bSFull + sb), k & 1u, ab, kErrTimeoutS));
+      if (!ok) break;
+      ptx::tc_fence_after_sync();
+      uint32_t su[16];
+      ptx::tmem_ld16(tS, su);
       float x[kDTRows];
 #pragma unroll
       for (int n = 0; n < kDTRows; ++n) {
-        const bool vis = kvalid && rvalid[n] && (!p.causal || pos <= qpos[n]);
+        const bool vis = all_vis ? (n < nrows) : (kvalid && n < nrows && (!p.causal || pos <= sqpos[n]));
         x[n] = vis ? __uint_as_float(su[n]) * sl2 : -INFINITY;
       }
-      // block maximum per query row: 16 shuffles per warp, then the 4 warps
+      // the tile's maximum per query row: 16 shuffles per warp, then 4 warps
       const float wm = warp_reduce16<true>(x, lane);
-      float* rbuf = red + sb * 4 * kDTRows;
-      if ((lane & 1) == 0) rbuf[warp * kDTRows + reduced_row(lane)] = wm;
+      if ((lane & 1) == 0) rbuf[wq * kDTRows + reduced_row(lane)] = wm;
       ptx::mbar_arrive(bar(L::bXch + sb));
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bXch + sb), (j >> 1) & 1u, ab, kErrTimeoutS));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bXch + sb), k & 1u, ab, kErrTimeoutS));
       if (!ok) break;
-      float alpha[kDTRows], muse[kDTRows];
+      float alpha[kDTRows];
       bool any_rescale = false;
 #pragma unroll
       for (int n = 0; n < kDTRows; ++n) {
         const float tmax = fmaxf(fmaxf(rbuf[n], rbuf[kDTRows + n]), fmaxf(rbuf[2 * kDTRows + n], rbuf[3 * kDTRows + n]));
         const float m_new = fmaxf(m_run[n], tmax);
-        muse[n] = (m_new == -INFINITY) ? 0.f : m_new;
         alpha[n] = (m_run[n] == m_new) ? 1.f : ptx::ex2(m_run[n] - m_new);
         any_rescale |= (alpha[n] != 1.f) && (m_run[n] != -INFINITY);
         m_run[n] = m_new;
       }
-      // probabilities: this thread's column of P^T (bf16) and its share of l;
-      // the buffer was last read by the P V of tile j - 2
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone + sb), ((j - 2) >> 1) & 1u, ab, kErrTimeoutO));
+      // the P buffer and the accumulator were last used by this pipeline's
+      // previous tile, whose P V must have run
+      if (k >= 1) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone + sb), (k - 1) & 1u, ab, kErrTimeoutO));
         if (!ok) break;
+        ptx::tc_fence_after_sync();
       }
-      uint8_t* pbuf = smem + L::kP + sb * L::kPBuf;
+      // probabilities: this thread's column of P^T (bf16 head and remainder)
+      // and its share of l
 #pragma unroll
       for (int n = 0; n < kDTRows; ++n) {
-        const float pr = (x[n] == -INFINITY) ? 0.f : ptx::ex2(x[n] - muse[n]);
+        const float muse = (m_run[n] == -INFINITY) ? 0.f : m_run[n];
+        const float pr = (x[n] == -INFINITY) ? 0.f : ptx::ex2(x[n] - muse);
         lpart[n] = lpart[n] * alpha[n] + pr;
         const __nv_bfloat16 hi = __float2bfloat16_rn(pr);
         *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128_offset(n, t, L::kPBox)) = hi;
         *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128_offset(kDTRows + n, t, L::kPBox)) =
             __float2bfloat16_rn(pr - __bfloat162float(hi));
       }
-      // rescale this thread's column of O^T when a row's maximum rose, once
-      // the previous P V has run (otherwise nothing waits for it)
-      if (j >= 1 && any_rescale) {
-        ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1u, ab,
-                                              kErrTimeoutO));
-        if (!ok) break;
-        ptx::tc_fence_after_sync();
-        {
-          uint32_t u[32];
-          ptx::tmem_ld32(tO, u);
+      // this thread's column of the accumulator, when a row's maximum rose
+      if (any_rescale) {
+        uint32_t u[16];
+        ptx::tmem_ld16(tO, u);
 #pragma unroll
-          for (int n = 0; n < kDTRows; ++n) {
-            u[n] = __float_as_uint(__uint_as_float(u[n]) * alpha[n]);
-            u[kDTRows + n] = __float_as_uint(__uint_as_float(u[kDTRows + n]) * alpha[n]);
-          }
-          ptx::tmem_st32(tO, u);
-          ptx::tmem_wait_st();
-        }
+        for (int n = 0; n < kDTRows; ++n) u[n] = __float_as_uint(__uint_as_float(u[n]) * alpha[n]);
+        ptx::tmem_st16(tO, u);
+        ptx::tmem_ld16(tO + kDTRows, u);
+#pragma unroll
+        for (int n = 0; n < kDTRows; ++n) u[n] = __float_as_uint(__uint_as_float(u[n]) * alpha[n]);
+        ptx::tmem_st16(tO + kDTRows, u);
+        ptx::tmem_wait_st();
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before_sync();
@@ -446,47 +458,78 @@ __global__ void __launch_bounds__(kDTThreads, 1)
     }
 
     // ---- epilogue: the block's partial state ------------------------------
-    if (ok && J > 0) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone + ((J - 1) & 1)), ((J - 1) >> 1) & 1u, ab,
-                                            kErrTimeoutO));
+    // this pipeline's last P V (and with it every product issued before it)
+    if (ok && k > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bPVDone + sb), (k - 1) & 1u, ab, kErrTimeoutO));
       if (ok) ptx::tc_fence_after_sync();
     }
+    float* const comb = reinterpret_cast<float*>(smem + L::kComb);
     if (ok) {
-      // row sums over the 128 threads, reusing the exchange buffers in warp order
+      // this pipeline's row sums over its 128 threads
       const float ws = warp_reduce16<false>(lpart, lane);
-      float* rbuf = red + (J & 1) * 4 * kDTRows;
-      if ((lane & 1) == 0) rbuf[warp * kDTRows + reduced_row(lane)] = ws;
-      ptx::mbar_arrive(bar(L::bXch + (J & 1)));
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bXch + (J & 1)), (J >> 1) & 1u, ab, kErrTimeoutS));
-      if (ok) {
-        uint32_t u[32];
-        ptx::tmem_ld32(tO, u);
+      if ((lane & 1) == 0) rbuf[wq * kDTRows + reduced_row(lane)] = ws;
+      ptx::mbar_arrive(bar(L::bXch + sb));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::bXch + sb), k & 1u, ab, kErrTimeoutS));
+      if (ok && t < kDTRows) {
+        float mr = -INFINITY;
 #pragma unroll
-        for (int n = 0; n < kDTRows; ++n) {
-          if (n >= nrows) break;
-          const int rr = row0 + n;
-          const int h = g * G + rr / p.R;
-          const int tok = rr % p.R;
-          // partial layout: o [P, B, R, Hq, D]; m, l [P, B, Hq, R]
-          p.part_o[(((static_cast<long long>(pi) * p.B + b) * p.R + tok) * p.Hq + h) * kDTD + t] =
-              __uint_as_float(u[n]) + __uint_as_float(u[kDTRows + n]);
-        }
-        if (t < nrows) {
-          const int n = t;
-          float lsum = 0.f;
-          float mr = -INFINITY;
+        for (int n = 0; n < kDTRows; ++n)
+          if (n == t) mr = m_run[n];
+        comb[(sb * 2 + 0) * kDTRows + t] = mr;
+        comb[(sb * 2 + 1) * kDTRows + t] =
+            rbuf[t] + rbuf[kDTRows + t] + rbuf[2 * kDTRows + t] + rbuf[3 * kDTRows + t];
+      }
+    }
+    // the two pipelines' states meet here (a pipeline that gave up still
+    // arrives, so the other never waits in vain)
+    ptx::tc_fence_before_sync();
+    ptx::named_bar_sync(1, 256);
+    ptx::tc_fence_after_sync();
+    if (sb == 0 && ok && !*abort_flag) {
+      // o = o0 * 2^(m0 - M) + o1 * 2^(m1 - M), l likewise, M = max(m0, m1)
+      float f0[kDTRows], f1[kDTRows];
 #pragma unroll
-          for (int w = 0; w < 4; ++w) lsum += rbuf[w * kDTRows + n];
+      for (int n = 0; n < kDTRows; ++n) {
+        const float m0 = comb[n], m1 = comb[2 * kDTRows + n];
+        const float M = fmaxf(m0, m1);
+        f0[n] = (m0 == -INFINITY) ? 0.f : ptx::ex2(m0 - M);
+        f1[n] = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - M);
+      }
+      const uint32_t tO1 = tO + 2 * kDTRows;
+      float acc[kDTRows];
+      uint32_t u[16];
+      ptx::tmem_ld16(tO, u);
 #pragma unroll
-          for (int k = 0; k < kDTRows; ++k)
-            if (k == n) mr = m_run[k];
-          const int rr = row0 + n;
-          const int h = g * G + rr / p.R;
-          const int tok = rr % p.R;
-          const long long pm = ((static_cast<long long>(pi) * p.B + b) * p.Hq + h) * p.R + tok;
-          p.part_m[pm] = mr;
-          p.part_l[pm] = lsum;
-        }
+      for (int n = 0; n < kDTRows; ++n) acc[n] = __uint_as_float(u[n]) * f0[n];
+      ptx::tmem_ld16(tO + kDTRows, u);
+#pragma unroll
+      for (int n = 0; n < kDTRows; ++n) acc[n] = fmaf(__uint_as_float(u[n]), f0[n], acc[n]);
+      ptx::tmem_ld16(tO1, u);
+#pragma unroll
+      for (int n = 0; n < kDTRows; ++n) acc[n] = fmaf(__uint_as_float(u[n]), f1[n], acc[n]);
+      ptx::tmem_ld16(tO1 + kDTRows, u);
+#pragma unroll
+      for (int n = 0; n < kDTRows; ++n) acc[n] = fmaf(__uint_as_float(u[n]), f1[n], acc[n]);
+#pragma unroll
+      for (int n = 0; n < kDTRows; ++n) {
+        if (n >= nrows) break;
+        const int rr = row0 + n;
+        const int h = g * G + rr / p.R;
+        const int tok = rr % p.R;
+        // partial layout: o [P, B, R, Hq, D]; m, l [P, B, Hq, R]
+        p.part_o[(((static_cast<long long>(pi) * p.B + b) * p.R + tok) * p.Hq + h) * kDTD + t] = acc[n];
+      }
+      if (t < nrows) {
+        const float m0 = comb[t], m1 = comb[2 * kDTRows + t];
+        const float M = fmaxf(m0, m1);
+        const float l = ((m0 == -INFINITY) ? 0.f : comb[kDTRows + t] * ptx::ex2(m0 - M)) +
+                        ((m1 == -INFINITY) ? 0.f : comb[3 * kDTRows + t] * ptx::ex2(m1 - M));
+        const int rr = row0 + t;
+        const int h = g * G + rr / p.R;
+        const int tok = rr % p.R;
+        const long long pm = ((static_cast<long long>(pi) * p.B + b) * p.Hq + h) * p.R + tok;
+        p.part_m[pm] = M;
+        p.part_l[pm] = l;
       }
     }
   }

@@ -413,6 +413,7 @@ def test_allgather_large_sampled_rows():
     (3000, 5, "zigzag", 3, 6, 3, 128, 1),        # zig-zag chunks of 300 keys: two ragged tiles per shard
     (6200, 4, "zigzag", 2, 8, 1, 128, 2),        # chunks of 775 keys, batch 2
     (2600, 4, "contiguous", 2, 8, 2, 64, 1),     # D = 64 (warp-level kernel), contiguous
+    (2048, 4, "zigzag", 4, 64, 8, 128, 4),       # 64 (batch, head, row block) units, 3 partials each
     (131072, 16, "zigzag", 1, 16, 1, 128, 1),    # the s128k shape: 16 query heads share one KV head
 ])
 def test_decode_split_kv_full_parity(S, c, layout, R, Hq, Hkv, D, B):
