@@ -442,6 +442,9 @@ def run_decode(args, rank, world, local):
     graph_ms = timed(graph.replay)
     tiny_graph_ms = timed(tiny_graph.replay)
     ra.device_error()
+    # For scale: the device reading the same K and V bytes with two library
+    # reductions (torch.sum over K, then over V), timed the same way.
+    read_ms = timed(lambda: (k.sum(), v.sum()))
     nbytes = 2 * k.numel() * k.element_size() + 2 * q.numel() * q.element_size() + w.B * w.Hq * 4
     peaks, kind = load_peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
@@ -457,6 +460,8 @@ def run_decode(args, rank, world, local):
                    "graph_ms_per_step": graph_ms,
                    "gbs_graph": nbytes / (graph_ms * 1e-3) / 1e9,
                    "one_kernel_graph_ms": tiny_graph_ms,
+                   "torch_sum_k_then_v_ms": read_ms,
+                   "gbs_torch_sum_k_then_v": nbytes / (read_ms * 1e-3) / 1e9,
                    "ms_per_step_write_only_flush": ms_dirty,
                    "gbs_write_only_flush": nbytes / (ms_dirty * 1e-3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),

@@ -693,18 +693,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int orow = row_ok ? qpos : 0;
         const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
         const long long obase = ((static_cast<long long>(b) * p.S_out + orow) * p.Hq + h) * D;
+        // the output is written once and not read here: evict first, so that
+        // it does not push the key and value tiles (read by every pair) out
+        // of L2
+        const uint64_t opol = ptx::l2_policy_evict_first();
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t u[32];
           ptx::tmem_ld32(tO + cc * 32, u);
           if (row_ok && p.out_f32) {
-            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + cc * 32);
+            float* d = static_cast<float*>(p.out) + obase + cc * 32;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(u[4 * i]) * inv_l, __uint_as_float(u[4 * i + 1]) * inv_l,
-                                  __uint_as_float(u[4 * i + 2]) * inv_l, __uint_as_float(u[4 * i + 3]) * inv_l);
+              ptx::st_global_v4_hint(d + 4 * i,
+                                     make_uint4(__float_as_uint(__uint_as_float(u[4 * i]) * inv_l),
+                                                __float_as_uint(__uint_as_float(u[4 * i + 1]) * inv_l),
+                                                __float_as_uint(__uint_as_float(u[4 * i + 2]) * inv_l),
+                                                __float_as_uint(__uint_as_float(u[4 * i + 3]) * inv_l)),
+                                     opol);
           } else if (row_ok) {
-            uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
+            __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(p.out) + obase + cc * 32;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               uint4 w;
@@ -712,7 +720,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               w.y = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv_l, __uint_as_float(u[8 * i + 3]) * inv_l);
               w.z = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv_l, __uint_as_float(u[8 * i + 5]) * inv_l);
               w.w = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv_l, __uint_as_float(u[8 * i + 7]) * inv_l);
-              d4[i] = w;
+              ptx::st_global_v4_hint(d + 8 * i, w, opol);
             }
           }
         }
