@@ -466,8 +466,7 @@ def run_decode(args, rank, world, local):
                    "gbs_write_only_flush": nbytes / (ms_dirty * 1e-3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
                      "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
-                     "kernel": ("decode_tc_kernel + decode_merge_kernel" if w.D == 128
-                                else "decode_partial_kernel + decode_merge_kernel")},
+                     "kernel": "decode_tc_kernel + decode_merge_kernel"},
         "gpu_launches": 2 * args.steps}), flush=True)
 
 

@@ -8,9 +8,10 @@
 // 128-key tiles (tile pi, pi + P, ... over all shards' tiles), and writes one
 // partial online-softmax state (o, m, l) for them.  The 16 query rows are too
 // few for the M of tcgen05.mma, so the products are taken transposed, with the
-// 128 keys (or the 128 output columns) as M and the 16 query rows as N:
+// 128 keys (or the output columns) as M = 128 and the 16 query rows as N:
 //   S^T = K Q^T        A = K tile (K-major), B = Q (K-major)      -> TMEM, lane = key
 //   O^T += V^T P^T     A = V tile read M-major, B = P^T (K-major) -> TMEM, lane = column
+// (head dimension D = 128 or 64; for D = 64 lanes 64-127 of O^T are unused).
 // Each softmax thread owns one key of the tile (one TMEM lane): it scales and
 // masks its 16 scores, the block's maximum per query row is reduced across the
 // 128 threads (shuffles, then four warps through shared memory), it writes its
@@ -24,8 +25,8 @@
 // softmax pipelines (warps 0-3 and 4-7) take the block's tiles in turn, each
 // with its own S and P buffers, O^T accumulator and online-softmax state, so
 // that one works on a tile while the other's product runs; their two states
-// are merged at the end of the block.  K and V tiles stream through three shared-memory
-// stages by TMA (a striped shard's keys, every c-th row, through a 5-D view of
+// are merged at the end of the block.  K and V tiles stream through three
+// shared-memory stages by TMA (a striped shard's keys, every c-th row, through a 5-D view of
 // the tensor), so the block reads each key and value byte once, and the
 // kernel is bound by HBM bandwidth; the loads carry an evict-first L2 policy,
 // so that the stream displaces its own lines rather than whatever else L2
@@ -53,7 +54,6 @@ namespace {
 
 constexpr int kDTRows = 16;           // query rows per block: the MMAs' N
 constexpr int kDTKeys = 128;          // keys per tile
-constexpr int kDTD = 128;             // head dimension of this kernel
 constexpr int kDTStages = 3;
 constexpr int kDTWarpLoad = 8;
 constexpr int kDTWarpMma = 9;
@@ -61,18 +61,27 @@ constexpr int kDTThreads = 10 * 32;
 constexpr uint32_t kDTTmemCols = 128;  // S0 | S1 (16 columns each) | O0 | O1 (heads, remainders: 32 each)
 constexpr int kDTTargetBlocks = 152;  // one resident block per SM
 
+// Shared memory of the kernel for head dimension D (64 or 128).
+template <int D>
 struct DTSmem {
   static constexpr int kBox = 64;                            // bf16 columns per 128-byte row
+  static constexpr int kNB = D / kBox;                       // column boxes per key or value row
   static constexpr int kKVBox = kDTKeys * kBox * 2;          // 16 KB: 128 keys x 64 columns
-  static constexpr int kKVTile = 2 * kKVBox;                 // 32 KB: 128 keys x 128 columns
+  static constexpr int kKVTile = kNB * kKVBox;               // 128 keys x D columns
   static constexpr int kRowsBox = kDTRows * kBox * 2;        // 2 KB: 16 rows x 64 columns
-  static constexpr int kQ = 0;                               // Q: 16 rows x 128 columns (2 boxes)
+  static constexpr int kQ = 0;                               // Q: 16 rows x D columns (kNB boxes)
   static constexpr int kPBox = 2 * kRowsBox;                 // 4 KB: 32 rows (16 heads, 16 remainders) x 64 keys
   static constexpr int kPBuf = 2 * kPBox;                    // P^T for the 128 keys of a tile
   static constexpr int kP = kQ + 2 * kRowsBox;               // two such buffers
-  static constexpr int kK = kP + 2 * kPBuf;
-  static constexpr int kV = kK + kDTStages * kKVTile;
-  static constexpr int kBar = kV + kDTStages * kKVTile;
+  static constexpr int kV = kP + 2 * kPBuf;
+  static constexpr int kK = kV + kDTStages * kKVTile;
+  static constexpr int kBar = kK + kDTStages * kKVTile;
+  // O^T += V^T P^T reads V^T as an M = 128 operand: its rows 64-127 are the
+  // second column box of the value tile (D = 128), or, for D = 64, whatever
+  // lies one offset further -- the same stage's key tile -- which only fills
+  // O^T lanes 64-127, never read (a row of the product depends only on its
+  // own row of A)
+  static constexpr int kVLbo = (D == 128) ? kKVBox : (kK - kV);
   static constexpr int bKVFull = 0;
   static constexpr int bKVEmpty = bKVFull + kDTStages;
   static constexpr int bSFull = bKVEmpty + kDTStages;
@@ -89,6 +98,8 @@ struct DTSmem {
   static constexpr int kDynamic = kBytes + 1024;
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kP % 1024 == 0, "swizzle atoms are 1024 bytes");
   static_assert(kDynamic <= 232448, "shared memory budget");
+  static_assert(D == 64 || D == 128, "head dimension");
+  static_assert(kVLbo % 16 == 0 && kVLbo / 16 < 16384, "leading byte offset field");
 };
 
 __device__ __forceinline__ long long dt_natural_key(int r, int i, int n, int c, int layout) {
@@ -149,10 +160,11 @@ __device__ __forceinline__ int reduced_row(int lane) {
   return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
+template <int D>
 __global__ void __launch_bounds__(kDTThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p) {
-  using L = DTSmem;
+  using L = DTSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -223,24 +235,28 @@ __global__ void __launch_bounds__(kDTThreads, 1)
   int* const sqpos = reinterpret_cast<int*>(smem + L::kQpos);
   if (threadIdx.x < kDTRows)
     sqpos[threadIdx.x] = (static_cast<int>(threadIdx.x) < nrows) ? p.q_pos[(row0 + threadIdx.x) % p.R] : INT_MIN;
-  // Q: 16 rows x 128 columns, K-major with the 128-byte swizzle; row
+  // Q: 16 rows x D columns, K-major with the 128-byte swizzle; row
   // n = (head within group) * R + token, rows past the block's rows are zero.
   if (warp < 4) {
+    constexpr int kCols = D / 8;       // columns per thread: 8 threads per row
     const int t = threadIdx.x;
     const int n = t >> 3;              // row
-    const int d0 = (t & 7) * 16;       // 16 columns
-    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = make_uint4(0, 0, 0, 0);
+    const int d0 = (t & 7) * kCols;
+    uint4 w[kCols / 8];
+#pragma unroll
+    for (int i = 0; i < kCols / 8; ++i) w[i] = make_uint4(0, 0, 0, 0);
     if (n < nrows) {
       const int rr = row0 + n;
       const int h = g * G + rr / p.R;
       const int tok = rr % p.R;
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                        ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * kDTD + d0);
-      w0 = src[0];
-      w1 = src[1];
+                                                        ((static_cast<long long>(b) * p.R + tok) * p.Hq + h) * D + d0);
+#pragma unroll
+      for (int i = 0; i < kCols / 8; ++i) w[i] = src[i];
     }
-    *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(n, d0, L::kRowsBox)) = w0;
-    *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(n, d0 + 8, L::kRowsBox)) = w1;
+#pragma unroll
+    for (int i = 0; i < kCols / 8; ++i)
+      *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(n, d0 + 8 * i, L::kRowsBox)) = w[i];
     ptx::fence_proxy_async_smem();
   }
   ptx::tc_fence_before_sync();
@@ -265,7 +281,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         ptx::mbar_arrive_expect_tx(bar(L::bKVFull + st), 2 * L::kKVTile);
         if (p.layout == RA_STRIPED) {
           // every c-th key: (column, head, shard, index in shard, batch)
-          for (int x = 0; x < 2; ++x) {
+          for (int x = 0; x < L::kNB; ++x) {
             ptx::tma_load_5d_hint(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
                                   x * L::kBox, g, shard, i0, b, pol);
             ptx::tma_load_5d_hint(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
@@ -273,7 +289,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
           }
         } else {
           const int nat0 = static_cast<int>(dt_natural_key(shard, i0, p.n, p.c, p.layout));
-          for (int x = 0; x < 2; ++x) {
+          for (int x = 0; x < L::kNB; ++x) {
             ptx::tma_load_4d_hint(sbase + L::kK + st * L::kKVTile + x * L::kKVBox, &tm_k, bar(L::bKVFull + st),
                                   x * L::kBox, g, nat0, b, pol);
             ptx::tma_load_4d_hint(sbase + L::kV + st * L::kKVTile + x * L::kKVBox, &tm_v, bar(L::bKVFull + st),
@@ -298,14 +314,14 @@ __global__ void __launch_bounds__(kDTThreads, 1)
       constexpr uint32_t idPV = ptx::idesc_bf16_f32(128, 2 * kDTRows, false, true);
       const uint64_t dQ = ptx::smem_desc_sw128(sbase + L::kQ, 16, 1024);
       const uint64_t dK = ptx::smem_desc_sw128(sbase + L::kK, 16, 1024);
-      const uint64_t dV = ptx::smem_desc_sw128(sbase + L::kV, L::kKVBox, 1024);
+      const uint64_t dV = ptx::smem_desc_sw128(sbase + L::kV, L::kVLbo, 1024);
       const uint64_t dP = ptx::smem_desc_sw128(sbase + L::kP, 16, 1024);
       bool ok = true;
       bool issued_any = false;
       auto issue_S = [&](int st, int sb) {
         const uint64_t kd = dK + static_cast<uint64_t>((st * L::kKVTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kDTD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t oa = static_cast<uint64_t>(((kk / 4) * L::kKVBox + (kk % 4) * 32) >> 4);
           const uint64_t ob = static_cast<uint64_t>(((kk / 4) * L::kRowsBox + (kk % 4) * 32) >> 4);
           ptx::tc_mma_ss(tmem + sb * kDTRows, kd + oa, dQ + ob, idS, kk > 0 ? 1u : 0u);
@@ -517,7 +533,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
         const int h = g * G + rr / p.R;
         const int tok = rr % p.R;
         // partial layout: o [P, B, R, Hq, D]; m, l [P, B, Hq, R]
-        p.part_o[(((static_cast<long long>(pi) * p.B + b) * p.R + tok) * p.Hq + h) * kDTD + t] = acc[n];
+        if (t < D) p.part_o[(((static_cast<long long>(pi) * p.B + b) * p.R + tok) * p.Hq + h) * D + t] = acc[n];
       }
       if (t < nrows) {
         const float m0 = comb[t], m1 = comb[2 * kDTRows + t];
@@ -547,7 +563,7 @@ __global__ void __launch_bounds__(kDTThreads, 1)
 
 bool decode_tc_applies(int D, int n, int layout) {
   (void)layout;
-  return D == kDTD && n > 0;
+  return (D == 64 || D == 128) && n > 0;
 }
 
 int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c, int layout) {
@@ -561,19 +577,19 @@ int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c, int layout) {
   return static_cast<int>((tiles + per - 1) / per);
 }
 
-int launch_decode_tc(const DecodeParams& p, void* stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+template <int D>
+int launch_decode_tc_d(const DecodeParams& p, cudaStream_t s) {
   CUtensorMap mk, mv;
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
   launch_stage() = "cuTensorMapEncodeTiled (decode)";
   int e = 0;
   if (p.layout == RA_STRIPED) {
-    e = make_tma_map_bf16_strided(&mk, p.k, p.B, p.S, p.Hkv, kDTD, p.c, kDTKeys);
-    if (!e) e = make_tma_map_bf16_strided(&mv, p.v, p.B, p.S, p.Hkv, kDTD, p.c, kDTKeys);
+    e = make_tma_map_bf16_strided(&mk, p.k, p.B, p.S, p.Hkv, D, p.c, kDTKeys);
+    if (!e) e = make_tma_map_bf16_strided(&mv, p.v, p.B, p.S, p.Hkv, D, p.c, kDTKeys);
   } else {
-    e = make_tma_map_bf16(&mk, p.k, p.B, p.S, p.Hkv, kDTD, kDTKeys);
-    if (!e) e = make_tma_map_bf16(&mv, p.v, p.B, p.S, p.Hkv, kDTD, kDTKeys);
+    e = make_tma_map_bf16(&mk, p.k, p.B, p.S, p.Hkv, D, kDTKeys);
+    if (!e) e = make_tma_map_bf16(&mv, p.v, p.B, p.S, p.Hkv, D, kDTKeys);
   }
   if (e) return e;
   static int done[64] = {0};
@@ -581,8 +597,8 @@ int launch_decode_tc(const DecodeParams& p, void* stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
   if (!done[dev]) {
     launch_stage() = "cudaFuncSetAttribute (decode tensor-core kernel)";
-    const cudaError_t ce = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                DTSmem::kDynamic);
+    const cudaError_t ce = cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                DTSmem<D>::kDynamic);
     if (ce != cudaSuccess) return static_cast<int>(ce);
     done[dev] = 1;
   }
@@ -590,8 +606,15 @@ int launch_decode_tc(const DecodeParams& p, void* stream) {
   const int row_blocks = (G * p.R + kDTRows - 1) / kDTRows;
   dim3 grid(static_cast<unsigned>(p.B * p.Hkv * row_blocks), static_cast<unsigned>(p.P));
   launch_stage() = "decode tensor-core kernel launch";
-  decode_tc_kernel<<<grid, kDTThreads, DTSmem::kDynamic, s>>>(mk, mv, p);
+  decode_tc_kernel<D><<<grid, kDTThreads, DTSmem<D>::kDynamic, s>>>(mk, mv, p);
   return static_cast<int>(cudaGetLastError());
+}
+
+int launch_decode_tc(const DecodeParams& p, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.D == 128) return launch_decode_tc_d<128>(p, s);
+  if (p.D == 64) return launch_decode_tc_d<64>(p, s);
+  return static_cast<int>(cudaErrorInvalidValue);
 }
 
 }  // namespace ra

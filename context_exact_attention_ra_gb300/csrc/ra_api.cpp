@@ -527,7 +527,7 @@ ra_status ra_ring_forward(const void* q, const void* k, const void* v, ra_shape 
 }
 
 namespace {
-// Partials of a decode call: one per block over the c * pieces-per-shard pieces.
+// Partials of a decode call: one per block over the shards' 128-key tiles.
 struct DecodeWs {
   int P;
   size_t o, m, l, total;
@@ -536,9 +536,7 @@ struct DecodeWs {
 DecodeWs decode_ws(const ra_shape& s, int c, int layout) {
   DecodeWs w;
   const int n = s.Sk / c;
-  w.P = ra::decode_tc_applies(s.D, n, layout)
-            ? ra::decode_tc_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, n, c, layout)
-            : ra::decode_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, c * ra::decode_pieces_per_shard(n));
+  w.P = ra::decode_tc_partials(s.B, s.Hkv, s.Hq / s.Hkv, s.Sq, n, c, layout);
   const size_t P = static_cast<size_t>(w.P), B = static_cast<size_t>(s.B), R = static_cast<size_t>(s.Sq);
   size_t off = 0;
   w.o = off;  off = round_up(off + P * B * R * s.Hq * s.D * sizeof(float));
@@ -595,7 +593,6 @@ ra_status ra_decode_forward(const void* q, const int32_t* q_pos, const void* k, 
   p.q_pos = q_pos;
   p.k = k;
   p.v = v;
-  p.pieces_per_shard = ra::decode_pieces_per_shard(p.n);
   p.P = w.P;
   p.part_o = at<float>(workspace, w.o);
   p.part_m = at<float>(workspace, w.m);

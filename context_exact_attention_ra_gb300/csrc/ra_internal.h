@@ -74,8 +74,7 @@ struct DecodeParams {
   const int32_t* q_pos;        // [R] their global positions
   const void* k;               // [B, S, Hkv, D] bf16, natural order
   const void* v;
-  int pieces_per_shard;        // shard-local pieces of the key range
-  int P;                       // partials per query row (blocks over the c * pieces_per_shard pieces)
+  int P;                       // partials per query row (blocks over the shards' 128-key tiles)
   float* part_o;               // [P, B, R, Hq, D]
   float* part_m;               // [P, B, Hq, R] (base-2 units)
   float* part_l;
@@ -131,12 +130,9 @@ int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype,
                  float* lse, const int32_t* out_row, int S_out, void* stream);
 int launch_zero(void* ptr, size_t bytes, void* stream);
 int launch_decode(const DecodeParams& p, void* stream);
-int decode_pieces_per_shard(int n);
-// Number of partial states (blocks per batch, key/value head and row block).
-int decode_partials(int B, int Hkv, int G, int R, int pieces);
-// The tensor-core decode (decode_tc_sm103.cu): D = 128, every layout (each
-// contiguous stretch of a shard tiled on its own, striped shards through a
-// strided view); D = 64 runs the warp-level kernel.
+// The tensor-core decode (decode_tc_sm103.cu): D = 64 or 128, every layout
+// (each contiguous stretch of a shard tiled on its own, striped shards through
+// a strided view).
 bool decode_tc_applies(int D, int n, int layout);
 int decode_tc_partials(int B, int Hkv, int G, int R, int n, int c, int layout);
 int launch_decode_tc(const DecodeParams& p, void* stream);

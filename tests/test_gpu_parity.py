@@ -407,12 +407,13 @@ def test_allgather_large_sampled_rows():
 @pytest.mark.parametrize("S,c,layout,R,Hq,Hkv,D,B", [
     (4096, 4, "zigzag", 1, 8, 2, 128, 1),        # one new token, GQA 4:1
     (4096, 4, "contiguous", 4, 8, 2, 128, 2),    # a few tokens at mixed positions, batch 2
-    (3000, 5, "striped", 3, 6, 3, 64, 1),        # ragged pieces, D = 64 (warp-level kernel)
+    (3000, 5, "striped", 3, 6, 3, 64, 1),        # ragged last tile, D = 64
     (3000, 5, "striped", 3, 6, 3, 128, 1),       # striped shards on the tensor cores, ragged last tile
     (8192, 4, "striped", 1, 16, 1, 128, 2),      # striped, every tile full, batch 2
     (3000, 5, "zigzag", 3, 6, 3, 128, 1),        # zig-zag chunks of 300 keys: two ragged tiles per shard
     (6200, 4, "zigzag", 2, 8, 1, 128, 2),        # chunks of 775 keys, batch 2
-    (2600, 4, "contiguous", 2, 8, 2, 64, 1),     # D = 64 (warp-level kernel), contiguous
+    (2600, 4, "contiguous", 2, 8, 2, 64, 1),     # D = 64, contiguous
+    (2400, 4, "zigzag", 1, 16, 1, 64, 2),        # D = 64, zig-zag chunks of 300 keys, batch 2
     (2048, 4, "zigzag", 4, 64, 8, 128, 4),       # 64 (batch, head, row block) units, 3 partials each
     (131072, 16, "zigzag", 1, 16, 1, 128, 1),    # the s128k shape: 16 query heads share one KV head
 ])
