@@ -270,6 +270,112 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams mp) {
   }
 }
 
+// Two to four partials: one warp per few_rows(P) rows, every load of the warp --
+// each partial's o rows, and its m and l (one lane per (partial, row) pair) --
+// issued before any of them is used, so a warp waits for memory once.  Then
+// per row M = max_p m_p, w_p = 2^(m_p - M) (one lane each), L = sum_p w_p l_p
+// and out = sum_p w_p o_p / L, lse = ln 2 (M + log2 L): the same sums as
+// merge_kernel, in the same order over the partials.
+// rows per warp: four (two for four partials, to stay within 64 registers)
+__host__ __device__ constexpr int few_rows(int P) { return P == 4 ? 2 : 4; }
+
+template <int D, int P>
+__global__ void __launch_bounds__(256, 4) merge_few_kernel(const MergeParams mp) {
+  constexpr int V = D / 32;   // floats per lane
+  constexpr int R = few_rows(P);
+  static_assert(P * R <= 32, "one lane per (partial, row) pair");
+  const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(mp.B) * mp.Hq * mp.S;
+  const long long row0 = warp_id * R;
+  if (row0 >= rows) return;
+  const int nlive = static_cast<int>(min(static_cast<long long>(R), rows - row0));
+  // o is [B, S, Hq, D]: the warp's rows are consecutive
+  float o[P][R][V];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const float* opp = mp.a.outs[p] + row0 * D + lane * V;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (r < nlive) {
+        if constexpr (V == 4) {
+          const float4 f = __ldcs(reinterpret_cast<const float4*>(opp + r * D));
+          o[p][r][0] = f.x; o[p][r][1] = f.y; o[p][r][2] = f.z; o[p][r][3] = f.w;
+        } else {
+          const float2 f = __ldcs(reinterpret_cast<const float2*>(opp + r * D));
+          o[p][r][0] = f.x; o[p][r][1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) o[p][r][i] = 0.f;
+      }
+    }
+  }
+  // lane k = p * R + r: m and l of partial p for row r, in [B, Hq, S]
+  const int kp = lane / R, kr = lane % R;
+  const long long krow = min(row0 + kr, rows - 1);
+  const long long q0 = krow / mp.Hq;
+  const int k_h = static_cast<int>(krow - q0 * mp.Hq);
+  const int k_s = static_cast<int>(q0 % mp.S);
+  const int k_b = static_cast<int>(q0 / mp.S);
+  float mk = -INFINITY, lk = 0.f;
+  if (kp < P && kr < nlive) {
+    const long long si = (static_cast<long long>(k_b) * mp.Hq + k_h) * mp.S + k_s;
+    mk = __ldg(mp.a.ms[kp] + si);
+    lk = __ldg(mp.a.ls[kp] + si);
+  }
+  // this lane's row maximum and weight
+  float Mk = -INFINITY;
+#pragma unroll
+  for (int p = 0; p < P; ++p) Mk = fmaxf(Mk, __shfl_sync(0xffffffffu, mk, p * R + kr));
+  const float wk = (mk == -INFINITY) ? 0.f : exp2f(mk - Mk);
+  const float lw = lk * wk;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    float L = 0.f;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const float w = __shfl_sync(0xffffffffu, wk, p * R + r);
+      L += __shfl_sync(0xffffffffu, lw, p * R + r);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(o[p][r][i], w, acc[i]);
+    }
+    const float M = __shfl_sync(0xffffffffu, Mk, r);
+    const int hh = __shfl_sync(0xffffffffu, k_h, r);
+    const int ss = __shfl_sync(0xffffffffu, k_s, r);
+    const int bb = __shfl_sync(0xffffffffu, k_b, r);
+    if (r >= nlive) continue;
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    const int orow = (mp.out_row != nullptr) ? mp.out_row[ss] : ss;
+    const long long od = ((static_cast<long long>(bb) * mp.S_out + orow) * mp.Hq + hh) * D + lane * V;
+    if (mp.out_dtype == RA_F32) {
+      float* op = static_cast<float*>(mp.out) + od;
+      if constexpr (V == 4)
+        *reinterpret_cast<float4*>(op) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+      else
+        *reinterpret_cast<float2*>(op) = make_float2(acc[0] * inv, acc[1] * inv);
+    } else {
+      __nv_bfloat16* op = static_cast<__nv_bfloat16*>(mp.out) + od;
+      if constexpr (V == 4) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo);
+        u.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(op) = u;
+      } else {
+        *reinterpret_cast<__nv_bfloat162*>(op) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+      }
+    }
+    if (lane == 0 && mp.lse != nullptr)
+      mp.lse[(static_cast<long long>(bb) * mp.Hq + hh) * mp.S_out + orow] =
+          (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
 // One partial (the per-step mode's last step): out = o / l and
 // lse = m + log2 l, with m in base-2 units -- the fused kernel's epilogue
 // arithmetic, so both modes agree bit for bit.  Each thread owns one 16-byte
@@ -418,6 +524,20 @@ int launch_merge(const MergeArgs& a, int B, int S, int Hq, int D, int out_dtype,
       finalize_kernel<64><<<static_cast<unsigned>(fblocks), threads, 0, s>>>(mp);
     else
       return static_cast<int>(cudaErrorInvalidValue);
+    return static_cast<int>(cudaGetLastError());
+  }
+  if (a.P <= 4 && (D == 128 || D == 64)) {
+    const long long fwarps = (rows + few_rows(a.P) - 1) / few_rows(a.P);
+    const unsigned fblocks = static_cast<unsigned>((fwarps * 32 + threads - 1) / threads);
+    if (D == 128) {
+      if (a.P == 2) merge_few_kernel<128, 2><<<fblocks, threads, 0, s>>>(mp);
+      else if (a.P == 3) merge_few_kernel<128, 3><<<fblocks, threads, 0, s>>>(mp);
+      else merge_few_kernel<128, 4><<<fblocks, threads, 0, s>>>(mp);
+    } else {
+      if (a.P == 2) merge_few_kernel<64, 2><<<fblocks, threads, 0, s>>>(mp);
+      else if (a.P == 3) merge_few_kernel<64, 3><<<fblocks, threads, 0, s>>>(mp);
+      else merge_few_kernel<64, 4><<<fblocks, threads, 0, s>>>(mp);
+    }
     return static_cast<int>(cudaGetLastError());
   }
   const long long warps = (rows + kMergeRows - 1) / kMergeRows;

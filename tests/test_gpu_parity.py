@@ -248,9 +248,10 @@ def test_block_attn_arbitrary_positions_and_state(dtype):
     assert int(work[0].item()) == pairs * B * Hq
 
 
-# P = 9 and 64 take the merge through more than one pass of per-partial weights
-# (eight partials per pass); D = 64 the two-column-per-lane form
-@pytest.mark.parametrize("P,D", [(1, 128), (3, 128), (9, 128), (64, 128), (9, 64)])
+# P = 2-4 take the all-loads-first merge, P = 9 and 64 the general merge
+# through more than one pass of per-partial weights (eight partials per pass);
+# D = 64 the two-column-per-lane forms
+@pytest.mark.parametrize("P,D", [(1, 128), (2, 128), (3, 128), (4, 128), (9, 128), (64, 128), (2, 64), (9, 64)])
 def test_lse_merge_of_key_splits_equals_full_attention(P, D):
     B, S, Hq, Hkv = 1, 512, 4, 1
     g = torch.Generator().manual_seed(11)
