@@ -16,7 +16,7 @@ single-device softmax attention written out:
     out_i  = sum_{j in V(i)} exp(s_ij - m_i) v[b,j,g,:] / l_i
     lse_i  = m_i + ln l_i
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   * the causal mask compares global token positions and is inclusive (a query
     sees its own key) - the quiz (questions 6, 8) and the plate only say that
     later tokens attend to earlier ones;
