@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -592,15 +593,16 @@ int launch_decode_tc_d(const DecodeParams& p, cudaStream_t s) {
     if (!e) e = make_tma_map_bf16(&mv, p.v, p.B, p.S, p.Hkv, D, kDTKeys);
   }
   if (e) return e;
-  static int done[64] = {0};
+  // the shared-memory opt-in, once per device (setting it twice is harmless)
+  static std::atomic<int> done[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
-  if (!done[dev]) {
+  if (!done[dev].load(std::memory_order_acquire)) {
     launch_stage() = "cudaFuncSetAttribute (decode tensor-core kernel)";
     const cudaError_t ce = cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 DTSmem<D>::kDynamic);
     if (ce != cudaSuccess) return static_cast<int>(ce);
-    done[dev] = 1;
+    done[dev].store(1, std::memory_order_release);
   }
   const int G = p.Hq / p.Hkv;
   const int row_blocks = (G * p.R + kDTRows - 1) / kDTRows;

@@ -417,6 +417,7 @@ def test_allgather_large_sampled_rows():
     (2400, 4, "zigzag", 1, 16, 1, 64, 2),        # D = 64, zig-zag chunks of 300 keys, batch 2
     (2048, 4, "zigzag", 4, 64, 8, 128, 4),       # 64 (batch, head, row block) units, 3 partials each
     (131072, 16, "zigzag", 1, 16, 1, 128, 1),    # the s128k shape: 16 query heads share one KV head
+    (131072, 16, "striped", 1, 16, 1, 128, 1),   # the same keys in striped shards (strided tensor map)
 ])
 def test_decode_split_kv_full_parity(S, c, layout, R, Hq, Hkv, D, B):
     g = torch.Generator().manual_seed(S + R)
