@@ -302,6 +302,19 @@ def run_ours(args, rank, world, local):
             "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
             "frac_of_nominal_dense": achieved / NOMINAL_BF16_DENSE_TFLOPS}
 
+    # The work the ring did, counted on the GPU by one more call outside the
+    # timed region: the tiles executed (diagonal tiles computed whole) next to
+    # the algorithmic FLOP, the load imbalance over the ranks, and the K/V bytes
+    # a ring over real devices would pass (derived, not timed).
+    _, _, info = ra.ring_forward(qd, kd, vd, w.c, layout, w.causal, args.mode, scale=w.scale, report=True)
+    ra.device_error()
+    tiles = sum(x["full"] + x["partial"] for row in info["per_rank_step"] for x in row)
+    work = {"algorithmic_flop": int(info["algorithmic_flop"]),
+            "executed_tiles": int(tiles), "tile": "128 query rows x 128 keys of one (batch, head)",
+            "executed_tile_flop": int(4 * w.D * 128 * 128 * tiles),
+            "imbalance_pairs": info["imbalance_pairs"], "imbalance_tiles": info["imbalance_tiles"],
+            "ring_kv_bytes": int(info["ring_kv_bytes"]), "ring_kv_bytes_sent": int(info["ring_kv_bytes_sent"])}
+
     # end to end through the C ABI with host buffers (copies inside the call)
     e2e = None
     if args.e2e_steps > 0:
@@ -346,6 +359,7 @@ def run_ours(args, rank, world, local):
             "pct_dense_bf16_peak": {"of_measured": value / world / peak * 100,
                                     "of_nominal_2250": value / world / NOMINAL_BF16_DENSE_TFLOPS * 100},
             "roofline": roof,
+            "work": work,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
