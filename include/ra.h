@@ -296,8 +296,10 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
 /* Decode over keys and values spread across c shards (tutorial section 7:
  * decode has one query per step, and attention over the distributed keys needs
  * a gather of partial results, like a FlashDecoding split-K): every shard's
- * keys are split into pieces, a partial state (o, m, l) is computed for each
- * piece, and the partials are merged into the normalised output.
+ * keys are cut into 128-key tiles (each contiguous stretch of a shard on its
+ * own), a block of the tensor-core kernel computes one partial state (o, m, l)
+ * over a fixed set of tiles, and the partials are merged in a fixed order into
+ * the normalised output.  D = 64 or 128; every layout.
  *   shp        B, Sq = R new tokens, Sk = S keys, Hq, Hkv, D, dtype (bf16), scale
  *   q          device [B, R, Hq, D] bf16;  q_pos device int32 [R] global positions
  *   k, v       device [B, S, Hkv, D] bf16, natural order; the shards are those of
