@@ -28,10 +28,11 @@ constexpr int kMergeThreads = kMergeWarps * 32;
 // flight per lane (up to 152 partials in one round of loads), and fold them:
 // the round's maximum by shuffles, each partial's weight on one lane, the
 // weighted sums; the warps' states are then combined, each warp's weight
-// computed by one lane.  Launched as a dependent of the partial kernel: the
-// block (256 threads, 56 registers) is small enough to become resident beside
-// a partial block, and waits for that grid to finish before it reads the
-// partials.
+// computed by one lane.  Launched as a programmatic dependent of the partial
+// kernel, whose blocks allow the launch as they finish: the block (256
+// threads, 56 registers) is small enough to become resident beside a partial
+// block still tearing down, and waits for that grid to finish before it reads
+// the partials.
 template <int D>
 __global__ void __maxnreg__(56) decode_merge_kernel(const DecodeParams p) {
   __shared__ float red_m[kMergeWarps];

@@ -264,7 +264,6 @@ __global__ void __launch_bounds__(kDTThreads, 1)
   __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled early
 
   if (warp == kDTWarpLoad) {
     // ===================== TMA loads of the K and V tiles =================
@@ -554,6 +553,13 @@ __global__ void __launch_bounds__(kDTThreads, 1)
   // ---- teardown -------------------------------------------------------------
   ptx::tc_fence_before_sync();
   __syncthreads();
+  // The merge (a programmatic dependent) may launch once every block has got
+  // here: its blocks then land on SMs that are free, spread over the GPU,
+  // rather than crowding the few SMs free at the start (where their loads of
+  // the partials ran slowly), and the launch itself still overlaps the last
+  // blocks' teardown.  The merge waits for this grid's completion before it
+  // reads.
+  asm volatile("griddepcontrol.launch_dependents;");
   if (warp == kDTWarpMma) {
     ptx::tc_fence_after_sync();
     ptx::tmem_dealloc(tmem, kDTTmemCols);
