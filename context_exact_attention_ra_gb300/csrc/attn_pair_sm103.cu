@@ -237,11 +237,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const PairAbort ab{abort_flag, ptx::mapa_shared(ptx::smem_u32(const_cast<int*>(abort_flag)), pr ^ 1u), p.err};
 
   // ---- which problem this pair owns -------------------------------------
-  const int bh = static_cast<int>(blockIdx.x >> 1);
-  const int b = bh / p.Hq;
-  const int h = bh % p.Hq;
-  const int g = h / p.G;
-  int yb = blockIdx.y;
+  // Blocks start roughly in the order of their linear index; that order runs
+  // over (batch, key/value head) outermost, then the query blocks (heaviest
+  // first), then the G query heads sharing the key/value head: the pairs in
+  // flight together read the keys and values of one head, which stay in L2.
+  const long long lin = static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x;
+  const long long pq = lin >> 1;                       // pair index; the CTA is lin & 1
+  const int hl = static_cast<int>(pq % p.G);
+  const long long rest = pq / p.G;
+  int yb = static_cast<int>(rest % gridDim.y);
+  const int bg = static_cast<int>(rest / gridDim.y);
+  const int g = bg % p.Hkv;
+  const int b = bg / p.Hkv;
+  const int h = g * p.G + hl;
   if (p.block_order != nullptr) yb = p.block_order[yb];
   const int rank = yb / p.q_blocks_per_rank;
   const int row0 = (yb % p.q_blocks_per_rank) * kPairBlockRows;   // local row of the pair's first row
