@@ -211,10 +211,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- which problem this block owns -----------------------------------
-  const int b = blockIdx.x / p.Hq;
-  const int h = blockIdx.x % p.Hq;
-  const int g = h / p.G;
-  int yb = blockIdx.y;
+  // Blocks start roughly in the order of their linear index: (batch, key/value
+  // head) outermost, then the query blocks (heaviest first), then the G query
+  // heads sharing the key/value head, so that the blocks in flight together
+  // read the keys and values of one head, which stay in L2.
+  const long long lin = static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x;
+  const int hl = static_cast<int>(lin % p.G);
+  const long long rest = lin / p.G;
+  int yb = static_cast<int>(rest % gridDim.y);
+  const int bg = static_cast<int>(rest / gridDim.y);
+  const int g = bg % p.Hkv;
+  const int b = bg / p.Hkv;
+  const int h = g * p.G + hl;
   if (p.block_order != nullptr) yb = p.block_order[yb];
   const int rank = yb / p.q_blocks_per_rank;
   const int row0 = (yb % p.q_blocks_per_rank) * kPairRows;   // local row of Q0
