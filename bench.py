@@ -259,9 +259,9 @@ def run_ours(args, rank, world, local):
     ra.device_error()
     # ra_ring_prepare: pack, tile ranges, heavy-first block order (every
     # workload here has more than one query block); ra_ring_attend: one
-    # launch, or state init + c steps + merge in per-step mode
+    # launch, or one launch per ring step in per-step mode
     prep_launches = 3
-    launches_per_step = prep_launches + (w.c + 2 if md == ra.MODE_PER_STEP else 1)
+    launches_per_step = prep_launches + (w.c if md == ra.MODE_PER_STEP else 1)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]

@@ -375,30 +375,26 @@ ra_status ra_ring_attend(ra_shape shp, int c, int layout, int causal, int mode, 
     }
     return launch_attn(p, shp, S, S, stream);
   }
-  // Per-step: state in the workspace, one launch per ring step, then out / l.
+  // Per-step: one launch per ring step, the state carried through the
+  // workspace between launches.  The first step starts from the empty state
+  // (out = 0, m = -inf, l = 0, set in the kernel rather than read back) and the
+  // last one ends with out / l and lse in its epilogue instead of storing the
+  // state -- the same arithmetic as the separate finalisation, so the result
+  // is bitwise the fused mode's either way.
   p.o_state = at<float>(workspace, w.o);
   p.m_state = at<float>(workspace, w.m);
   p.l_state = at<float>(workspace, w.l);
-  p.load_state = 1;
-  p.store_state = 1;
-  p.finalize = 0;
-  int e = ra::launch_state_init(shp.B, S, shp.Hq, shp.D, p.o_state, p.m_state, p.l_state, stream);
-  if (e) return cuda_fail(e, ra::launch_stage());
   for (int t = 0; t < c; ++t) {
     const Range step(step_name(t));
     p.t_begin = t;
     p.t_end = t + 1;
+    p.load_state = (t > 0) ? 1 : 0;
+    p.store_state = (t + 1 < c) ? 1 : 0;
+    p.finalize = (t + 1 < c) ? 0 : 1;
     st = launch_attn(p, shp, S, S, stream);
     if (st != RA_OK) return st;
   }
-  ra::MergeArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.P = 1;
-  a.outs[0] = p.o_state;
-  a.ms[0] = p.m_state;
-  a.ls[0] = p.l_state;
-  return cuda_status(ra::launch_merge(a, shp.B, S, shp.Hq, shp.D, out_dtype, out, lse, p.q_pos, S,
-                                      stream));
+  return RA_OK;
 }
 
 ra_status ra_ring_read_work(ra_shape shp, int c, int layout, int mode, const void* workspace,
@@ -653,12 +649,14 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
   p.o_state = at<float>(workspace, w.o);
   p.m_state = at<float>(workspace, w.m);
   p.l_state = at<float>(workspace, w.l);
-  p.load_state = 1;
-  p.store_state = 1;
+  // as in the per-step ring: the first step starts from the empty state, the
+  // last one writes out / l and lse from its epilogue
+  p.out = out;
+  p.out_f32 = (out_dtype == RA_F32) ? 1 : 0;
+  p.lse = lse;
+  p.S_out = S;
   if (causal && c * p.q_blocks_per_rank <= ra::kMaxOrderedBlocks && c * p.q_blocks_per_rank > 1)
     p.block_order = at<int32_t>(workspace, w.order);
-  int e = ra::launch_state_init(shp.B, S, shp.Hq, shp.D, p.o_state, p.m_state, p.l_state, stream);
-  if (e) return cuda_fail(e, "state init launch");
 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaStream_t xs = overlap ? static_cast<cudaStream_t>(copy_stream) : cs;
@@ -679,6 +677,9 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
     p.v = vbuf[t & 1];
     p.t_begin = t;
     p.t_end = t + 1;
+    p.load_state = (t > 0) ? 1 : 0;
+    p.store_state = (t + 1 < c) ? 1 : 0;
+    p.finalize = (t + 1 < c) ? 0 : 1;
     st = launch_attn(p, shp, S, S, stream);
     if (st != RA_OK) break;
     ce = cudaEventRecord(ev_comp[t & 1], cs);
@@ -704,16 +705,7 @@ ra_status ra_ring_forward_rotate(const void* q, const void* k, const void* v, ra
   if (ev_comp[0]) cudaEventDestroy(ev_comp[0]);
   if (ev_comp[1]) cudaEventDestroy(ev_comp[1]);
   if (ce != cudaSuccess) return cuda_fail(ce, "ring rotation copies");
-  if (st != RA_OK) return st;
-  ra::MergeArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.P = 1;
-  a.outs[0] = p.o_state;
-  a.ms[0] = p.m_state;
-  a.ls[0] = p.l_state;
-  ra::launch_stage() = "merge kernel launch";
-  return cuda_status(ra::launch_merge(a, shp.B, S, shp.Hq, shp.D, out_dtype, out, lse, p.q_pos, S,
-                                      stream));
+  return st;
 }
 
 size_t ra_ring_forward_hostio_workspace_size(ra_shape shp, int c, int layout, int mode,
