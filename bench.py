@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--workload", default="s128k")
     ap.add_argument("--layout", default=None)
     ap.add_argument("--mode", default="fused", choices=["fused", "per_step", "allgather"],
-                    help="fused ring (one launch), per-step launches + merge, or one step over all-gathered keys")
+                    help="fused ring (one launch), one launch per ring step, or one step over all-gathered keys")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -297,7 +297,7 @@ def run_ours(args, rank, world, local):
             "frac": achieved / peak, "traffic": kernel_traffic("attn_pair_sm103.cu") if md == ra.MODE_FUSED else None,
             "kernel": {ra.MODE_FUSED: "attn_fwd_pair_kernel (CTA pairs, D = 128)",
                        ra.MODE_ALLGATHER: "attn_fwd_pair_kernel (one step over the gathered keys)"}.get(
-                           md, "attend (per-step launches + merge)"),
+                           md, "attn_fwd_pair_kernel (one launch per ring step)"),
             "peak_source": f"{peak_kind} bf16_tflops (burst)",
             "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
             "frac_of_nominal_dense": achieved / NOMINAL_BF16_DENSE_TFLOPS}
