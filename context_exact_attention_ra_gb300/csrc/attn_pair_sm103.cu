@@ -56,6 +56,7 @@
 namespace ra {
 namespace {
 
+constexpr float kLazyMax = 1.f;   // log2 of the largest probability taken against a stale maximum
 constexpr int kWarpK = 8;
 constexpr int kWarpV = 9;
 constexpr int kWarpMmaS = 10;    // issues S = Q K^T (and allocates tensor memory)
@@ -610,7 +611,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(lbar(PL::bSFree + hh));
 
-        const float m_new = fmaxf(m_run, mx * sl2);
+        // The row's reference maximum moves only when the tile's maximum
+        // exceeds it by more than kLazyMax (base-2 units): below that the
+        // probabilities, taken against the old reference, stay at most
+        // 2^kLazyMax, and O and l need no rescaling.
+        // Every sum is kept against the same reference, so out = O / l and
+        // lse = m + log2 l are unchanged; the first visible key sets it.
+        const float m_cand = fmaxf(m_run, mx * sl2);
+        const float m_new = (m_cand - m_run > kLazyMax) ? m_cand : m_run;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = (m_run == m_new) ? 1.f : ptx::ex2(m_run - m_new);
         const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
